@@ -1,0 +1,391 @@
+"""Benchmark of the indexer top-k + page-table transform on GB300.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``
+
+One step is one pass of the whole path over one batch: the plan kernel and
+the select + transform kernels (``topk_plan`` + ``topk_transform``).  The
+headline workload is decode: batch 8192 x seq_len 8192 fp32 N(0,1) scores,
+k=512, page size 64, permuted page table (268 MB of scores, larger than L2;
+L2 is also flushed between timed steps).  ``value`` is HBM GB/s over the
+algorithmic bytes (scores read + seq_lens read + indices written, the page
+table excluded as in SGLang PR #26788), timed with CUDA events on the
+launching stream.  Secondary lines time the throughput (2048 x 65536, q.k
+scores), long-context (1/8/32 x 1M, k=2048) and ragged workloads.
+
+``--impl reference`` times the CPU oracle (full sort per row, all host cores)
+on a bounded sample of the same workload.  Under torchrun every rank runs the
+same per-GPU workload (weak scaling: rows are independent, no collective on
+the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_attention_indexer_uint32_gb300 import workloads  # noqa: E402
+
+METRIC = "top-k+page-transform HBM GB/s (fraction of peak); µs/call at batch 1, seq 1M"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_uint32_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the select kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"select_kernel_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != source_digest():
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if out.returncode == 0 and out.stdout.strip():
+                    self.samples.append([x.strip() for x in out.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        smax = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if len(s) > 4 + i and s[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def build_workload(name: str) -> workloads.Workload:
+    if name == "decode":
+        return workloads.decode()
+    if name == "throughput":
+        return workloads.throughput()
+    if name.startswith("long"):
+        return workloads.long_context(int(name[4:] or 1))
+    if name == "ragged":
+        return workloads.ragged()
+    if name == "tiny":
+        return workloads.tiny()
+    raise ValueError(name)
+
+
+def config_of(wl: workloads.Workload, name: str, world: int) -> dict:
+    eff = np.clip(wl.seq_lens.astype(np.int64), 0, wl.max_seq_len)
+    return {"workload": wl.name, "kind": name, "batch": wl.batch, "seq_len": int(eff.max()),
+            "sum_seq_len": int(eff.sum()), "k": wl.k, "page_size": wl.page_size, "row_stride": wl.row_stride,
+            "raw_output": wl.want_raw, "global_batch": wl.batch * world, "parallelism": f"replica{world}",
+            "l2": "flushed between timed steps (256 MB write); inputs > L2 for decode/throughput"}
+
+
+def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: bool):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_attention_indexer_uint32_gb300 import _lib, api
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    scores = torch.from_numpy(wl.scores).to(dev)
+    seq = torch.from_numpy(wl.seq_lens).to(dev)
+    table = torch.from_numpy(wl.page_table).to(dev)
+    out = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev)
+    raw = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev) if wl.want_raw else None
+    ws = torch.zeros(_lib.topk_plan_workspace_bytes(wl.batch), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws, stream)
+        _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
+                            wl.page_size, wl.k, out, raw, ws, stream)
+
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    n_long_launch = 1 if wl.max_seq_len > _threshold(wl.batch) else 0
+    launches_per_step = 2 + n_long_launch  # plan + short-row select (+ long-row cluster select)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local) if want_clocks else None
+    if sampler:
+        sampler.__enter__()
+    t_wall = time.perf_counter()
+    for e0, e1, e2 in ev:
+        flush.fill_(1.0)
+        e0.record(stream)
+        _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws, stream)
+        e1.record(stream)
+        _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
+                            wl.page_size, wl.k, out, raw, ws, stream)
+        e2.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.__exit__(None, None, None)
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
+    plan_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    sel_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flags = _lib.topk_read_flags(ws)
+    res = {"total_ms": total_ms, "step_ms": step_ms, "plan_ms": plan_ms, "select_ms": sel_ms,
+           "wall_s": t_wall, "flags": flags, "launches_per_step": launches_per_step,
+           "clocks": sampler.summary() if sampler else None}
+    del scores, flush
+    return res
+
+
+def _threshold(batch: int) -> int:
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    t = _lib.topk_get_tuning()
+    return t.long_threshold_small_batch if batch <= t.small_batch_max else t.long_threshold
+
+
+def time_e2e(wl, steps: int, warmup: int, local: int):
+    """Same metric through the public API from pinned host buffers: H2D copy of
+    the step's inputs, plan + transform, D2H copy of the result, every step."""
+    import torch
+
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    h_scores = torch.from_numpy(wl.scores).pin_memory()
+    h_seq = torch.from_numpy(wl.seq_lens).pin_memory()
+    h_table = torch.from_numpy(wl.page_table).pin_memory()
+    h_out = torch.empty((wl.batch, wl.k), dtype=torch.int32).pin_memory()
+    d_scores = torch.empty_like(h_scores, device=dev)
+    d_seq = torch.empty_like(h_seq, device=dev)
+    d_table = torch.empty_like(h_table, device=dev)
+    d_out = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev)
+    ws = torch.zeros(_lib.topk_plan_workspace_bytes(wl.batch), dtype=torch.uint8, device=dev)
+
+    def step():
+        d_scores.copy_(h_scores, non_blocking=True)
+        d_seq.copy_(h_seq, non_blocking=True)
+        d_table.copy_(h_table, non_blocking=True)
+        _lib.topk_plan(d_seq, wl.batch, wl.max_seq_len, ws, stream)
+        _lib.topk_transform(d_scores, wl.row_stride, d_seq, wl.batch, wl.max_seq_len, d_table,
+                            wl.page_table.shape[1], wl.page_size, wl.k, d_out, None, ws, stream)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    h2d = h_scores.numel() * 4 + h_seq.numel() * 4 + h_table.numel() * 4
+    d2h = h_out.numel() * 4
+    return ms, h2d, d2h
+
+
+def oracle_sample_time(wl, target_s: float = 12.0):
+    """Times the oracle (all host cores) on a bounded row sample of the workload."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    eff = np.clip(wl.seq_lens.astype(np.int64), 0, wl.max_seq_len)
+    # calibrate on a few rows, then size the sample for ~target_s of wall time
+    rows = np.arange(min(wl.batch, max(1, cores)))
+    t0 = time.perf_counter()
+    oracle.topk_transform(wl.scores[rows], wl.seq_lens[rows], wl.page_table[rows], wl.page_size, wl.k,
+                          max_seq_len=wl.max_seq_len, want_raw=False, nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(wl.batch, max(len(rows), len(rows) * target_s / dt)))
+    rows = np.arange(n)
+    t0 = time.perf_counter()
+    oracle.topk_transform(wl.scores[rows], wl.seq_lens[rows], wl.page_table[rows], wl.page_size, wl.k,
+                          max_seq_len=wl.max_seq_len, want_raw=False, nthreads=cores)
+    dt = time.perf_counter() - t0
+    nbytes = int(4 * eff[rows].sum() + 4 * n + 4 * n * wl.k)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.batch} rows of {wl.name}, {dt:.2f} s wall on {cores} threads"}
+
+
+def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: int, full: bool):
+    wl = build_workload(name)
+    nbytes = wl.algorithmic_bytes()
+    r = time_gpu(wl, steps, warmup, local, world, want_clocks=full)
+    peak, peak_kind = measured_peak()
+    ms_step = r["total_ms"] / steps
+    sel_avg = statistics.mean(r["select_ms"])
+    value = nbytes * world * steps / (r["total_ms"] / 1e3) / 1e9
+    achieved = nbytes / (sel_avg / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 scores, u32 keys, i32 indices", "data": "synthetic (seeded)",
+        "config": config_of(wl, name, world),
+        "us_per_call": round(ms_step * 1e3, 2),
+        "plan_us": round(statistics.mean(r["plan_ms"]) * 1e3, 2),
+        "select_us": round(sel_avg * 1e3, 2),
+        "algorithmic_bytes_per_step": nbytes,
+        "gpu_launches": r["launches_per_step"] * steps,
+        "device_flags": r["flags"],
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                     "kernel": "select_kernel (topk_transform), events around the call"},
+    }
+    if full:
+        e2e_steps = max(3, min(steps, 10))
+        ms, h2d, d2h = time_e2e(wl, e2e_steps, 2, local)
+        line["e2e"] = {"value": round(nbytes / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+        line["clocks"] = r["clocks"]
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = oracle_sample_time(wl)
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--secondary", default="throughput,long1,long8,long32,ragged",
+                    help="comma list of extra workloads timed after the headline one ('' for none)")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = build_workload(args.workload)
+        times, last = [], None
+        for _ in range(args.warmup):
+            oracle_sample_time(wl, target_s=2.0)
+        for _ in range(args.steps):
+            last = oracle_sample_time(wl, target_s=8.0)
+            times.append(last["value"])
+        v = statistics.mean(times)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 scores, i32 indices", "data": "synthetic (seeded)",
+            "config": config_of(wl, args.workload, 1),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = gpu_line(args.workload, args.steps, args.warmup, world, rank, local, full=True)
+    extra = []
+    for name in [s for s in args.secondary.split(",") if s]:
+        try:
+            sub = gpu_line(name, max(3, args.steps // 2), max(3, args.warmup // 2), world, rank, local, full=False)
+            extra.append({k: sub[k] for k in ("config", "value", "us_per_call", "select_us", "plan_us",
+                                              "roofline", "device_flags")})
+        except Exception as e:  # report, never hide
+            extra.append({"workload": name, "error": repr(e)})
+    line["secondary"] = extra
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,141 @@
+// topk_internal.h -- launch parameters, workspace layout and shared-memory
+// layout shared by the host dispatcher and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace topkidx {
+
+constexpr int kBins = 2048;             // bins per histogram round (11 bits)
+constexpr int kBinBits = 11;
+constexpr int kBinsX = kBins + 64;      // + control slots carried through cluster merges
+constexpr int kSlotOverflow = kBins;    // merged slot: some block's candidate buffer overflowed
+constexpr int kFinish = 32;             // a warp-wide compare-and-swap sort finishes <= 32 candidates
+constexpr int kSamplesPerThread = 4;    // gate samples held per thread
+constexpr int kItemsMax = 256;          // work items staged in shared memory per window
+constexpr int kMaxK = 2048;
+constexpr int kMaxCluster = 16;
+
+// Workspace written by the plan kernel.
+constexpr uint32_t kPlanMagic = 0x544f504bu;  // "TOPK"
+struct PlanHeader {
+    uint32_t magic;
+    int32_t batch;
+    int32_t max_seq_len;
+    int32_t long_threshold;
+    int32_t n_long;
+    int32_t n_short;
+    uint32_t flags;
+    int32_t reserved[9];
+};
+static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
+
+inline size_t plan_bytes(int32_t batch) {
+    if (batch < 1) return 0;
+    size_t b = sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(batch);
+    return (b + 255) / 256 * 256;
+}
+__host__ __device__ inline int32_t* plan_long_list(void* ws) {
+    return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(PlanHeader));
+}
+__host__ __device__ inline int32_t* plan_short_list(void* ws, int32_t batch) {
+    return plan_long_list(ws) + batch;
+}
+
+// Parameters of the select kernel (one block, or one cluster, per row).
+struct SelectParams {
+    const float* scores;
+    int64_t row_stride;
+    const int32_t* seq_lens;
+    int32_t batch;
+    int32_t max_seq_len;
+    const int32_t* page_table;
+    int64_t pt_stride;
+    int32_t log2_page;
+    int32_t k;
+    int32_t* out;
+    int32_t* raw_out;
+    const int32_t* items;     // row ids of this kernel's work list (nullptr: rows 0..n-1)
+    const int32_t* n_items_dev;  // device count of items (nullptr: n_items_host)
+    int32_t n_items_host;
+    const int32_t* items2;    // optional second list, taken after the first (nullptr: none)
+    const int32_t* n_items2_dev;
+    const PlanHeader* plan;   // the planned workspace (checked against batch / max_seq_len)
+    uint32_t* flags;          // device flag word (TOPK_FLAG_*)
+    int32_t tile;             // floats per bulk copy, multiple of 4
+    int32_t stages;           // bulk-copy ring depth
+    int32_t cap;              // candidate buffer entries per block
+    int32_t samples;          // gate samples per row
+    int32_t force_two_pass;
+    int32_t disable_gate;
+    uint64_t timeout_ns;
+};
+
+struct __align__(16) Control {
+    uint32_t ncand;       // candidates pushed in the current pass
+    uint32_t nemit;       // entries in the local emit list
+    uint32_t nfin;        // entries in the finish list
+    uint32_t smax;        // largest sample key
+    uint32_t res_bin, res_above, res_count, res_total;  // result of the last histogram scan
+    uint32_t rank_cnt[kMaxCluster];  // per-rank emitted counts (output placement)
+    uint32_t rank_eq[kMaxCluster];   // per-rank copies of the threshold key (tie quotas)
+    uint32_t err;
+    uint32_t pad[3];
+};
+
+struct Layout {
+    uint32_t ring, hist_a, hist_b, hist_m, cand_key, cand_idx, emit, fin_key, fin_idx, warp_tot, ctl;
+    uint32_t items_row, items_len, mbar, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int cluster, int tile, int stages, int cap, int k) {
+    Layout l;
+    uint32_t o = 0;
+    l.ring = o;
+    o = align_up(o + static_cast<uint32_t>(stages) * tile * 4u, 128);
+    l.hist_a = o;
+    o += kBinsX * 4u;
+    l.hist_b = o;
+    o += kBinsX * 4u;
+    l.hist_m = o;
+    o += cluster > 1 ? kBinsX * 4u : 0u;
+    l.cand_key = o;
+    o += static_cast<uint32_t>(cap) * 4u;
+    l.cand_idx = o;
+    o += static_cast<uint32_t>(cap) * 4u;
+    l.emit = o;
+    o += align_up(static_cast<uint32_t>(k), 4) * 4u;
+    l.fin_key = o;
+    o += kFinish * 4u;
+    l.fin_idx = o;
+    o += kFinish * 4u;
+    l.warp_tot = o;
+    o += 32 * 4u;
+    l.ctl = o;
+    o += align_up(sizeof(Control), 16);
+    l.items_row = o;
+    o += kItemsMax * 4u;
+    l.items_len = o;
+    o += kItemsMax * 4u;
+    l.mbar = align_up(o, 8);
+    o = l.mbar + 2u * stages * 8u;
+    l.total = align_up(o, 128);
+    return l;
+}
+
+// Host-side launchers (defined in topk_kernels.cu).
+cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
+                        void* workspace, cudaStream_t stream);
+cudaError_t launch_select(const SelectParams& p, int cluster, int grid_units, size_t smem, cudaStream_t stream);
+cudaError_t select_occupancy(int cluster, size_t smem, int* units_out);
+int select_threads(int cluster);
+cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
+                                  int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream);
+cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream);
+
+}  // namespace topkidx

@@ -1,0 +1,1094 @@
+// topk_kernels.cu -- sm_103a kernels of the indexer top-k + page-table
+// transform: the row-select kernel (one block, or one thread-block cluster,
+// per row), the plan kernel, the stand-alone page transform and the key map.
+//
+// Method (SGLang PR #26788 "[JIT Kernel] DeepSeek-V4 DSA indexer: faster
+// top-k + page-table transform (runtime k <= 2048)" and the DistRadixTopK
+// README "Ultra Low Latency Distributed Radix TopK Indexer Via NoC"): scores
+// are mapped to order-preserving uint32 keys, a radix histogram over the keys
+// finds the bin that holds the k-th largest key, later rounds refine that bin
+// over a shrinking candidate set, the last <= 32 candidates are finished by a
+// warp compare-and-swap sort, and a separate pass gathers the selected
+// positions through the page table.  Long rows are split over a cluster whose
+// blocks merge their histograms through distributed shared memory.
+//
+// GB300 choices (see the block comment above select_kernel): the row is
+// streamed once by the bulk-copy (TMA) engine into a shared-memory ring that
+// runs ahead across rows; a sampled gate keeps all but ~2k elements of a row
+// away from the histogram atomics; the gated elements are kept on chip, so a
+// second read of the row is only needed when they do not fit.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "topk_internal.h"
+#include "topkidx.h"
+
+namespace topkidx {
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+
+// ----------------------------------------------------------------- key map
+// Order-preserving fp32 -> uint32 map (DistRadixTopK README, "Distributed
+// Radix Sort via NoC", second point).  -0.0 is first folded onto +0.0 so the
+// two tie; then the sign bit is flipped for non-negative values and every
+// bit is flipped for negative ones, which makes unsigned key order equal to
+// IEEE order.  NaNs keep their bits: positive NaNs land above +inf, negative
+// NaNs below -inf.
+__device__ __forceinline__ uint32_t score_key(float x) {
+    uint32_t u = __float_as_uint(x);
+    u = (u == 0x80000000u) ? 0u : u;
+    const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u;
+    return u ^ m;
+}
+
+__device__ __forceinline__ int bit_length(uint32_t x) { return 32 - __clz(x); }
+
+__host__ __device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t min_i64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Shift that maps the key span [0, span] onto at most kBins bins.
+__device__ __forceinline__ int shift_for_span(uint32_t span) {
+    const int b = bit_length(span);
+    return b > kBinBits ? b - kBinBits : 0;
+}
+
+__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Warp-wide bitonic compare-and-swap sort, largest value to lane 0
+// (DistRadixTopK README, "Distributed Radix Sort via NoC", last point: once
+// the residual is down to a handful of candidates a CAS sort finishes it).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(kFull, v, j);
+            const bool lower = (lane & j) == 0;
+            const bool desc_seg = (lane & k) == 0;
+            const bool take_max = (lower == desc_seg);
+            v = take_max ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    return v;
+}
+
+__device__ __forceinline__ int32_t page_map(const int32_t* pt_row, int32_t log2_page, int32_t raw) {
+    if (raw < 0) return -1;
+    const uint32_t page = static_cast<uint32_t>(__ldg(pt_row + (raw >> log2_page)));
+    const uint32_t mask = (1u << log2_page) - 1u;
+    return static_cast<int32_t>((page << log2_page) + (static_cast<uint32_t>(raw) & mask));
+}
+
+struct ScanResult {
+    uint32_t bin, above, count, total;
+};
+
+struct Smem {
+    float* ring;
+    uint32_t* hist_a;
+    uint32_t* hist_b;
+    uint32_t* hist_m;
+    uint32_t* cand_key;
+    uint32_t* cand_idx;
+    uint32_t* emit;
+    uint32_t* fin_key;
+    uint32_t* fin_idx;
+    uint32_t* warp_tot;
+    Control* ctl;
+    int32_t* it_row;
+    int32_t* it_len;
+    uint64_t* full;
+    uint64_t* empty;
+};
+
+template <int NT>
+__device__ __forceinline__ void clear_hist(uint32_t* h, int tid) {
+    for (int i = tid * 4; i < kBinsX; i += NT * 4) *reinterpret_cast<uint4*>(h + i) = make_uint4(0, 0, 0, 0);
+}
+
+// Finds, in a histogram whose bins are ordered by key, the bin where the
+// count of elements taken from the top reaches `need`: returns that bin, the
+// count in the bins above it, its own count and the histogram total.  If the
+// total is below `need`, bin is 0xffffffff.  Every thread of the block must
+// call it; it contains two block barriers and reads `h` before the first.
+template <int NT>
+__device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need, int tid) {
+    constexpr int BPT = kBins / NT;
+    static_assert(BPT == 4 || BPT == 8, "bins per thread");
+    const int lane = tid & 31, warp = tid >> 5;
+    const int base = kBins - (tid + 1) * BPT;  // thread 0 owns the top bins
+    uint32_t v[BPT];
+#pragma unroll
+    for (int i = 0; i < BPT; i += 4) {
+        const uint4 q = *reinterpret_cast<const uint4*>(h + base + i);
+        v[i] = q.x;
+        v[i + 1] = q.y;
+        v[i + 2] = q.z;
+        v[i + 3] = q.w;
+    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) sum += v[i];
+    const uint32_t incl = warp_inclusive_sum(sum, lane);
+    if (lane == 31) s.warp_tot[warp] = incl;
+    if (tid == 0) s.ctl->res_bin = 0xffffffffu;
+    __syncthreads();
+    uint32_t pre = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const uint32_t t = s.warp_tot[w];
+        pre += (w < warp) ? t : 0u;
+        total += t;
+    }
+    const uint32_t excl = pre + incl - sum;
+    if (need > excl && need <= excl + sum) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = BPT - 1; i >= 0; --i) {
+            if (acc + v[i] >= need) {
+                s.ctl->res_bin = static_cast<uint32_t>(base + i);
+                s.ctl->res_above = acc;
+                s.ctl->res_count = v[i];
+                break;
+            }
+            acc += v[i];
+        }
+    }
+    __syncthreads();
+    ScanResult r;
+    r.bin = s.ctl->res_bin;
+    r.above = s.ctl->res_above;
+    r.count = s.ctl->res_count;
+    r.total = total;
+    return r;
+}
+
+// Sums the histograms of all blocks of the cluster (DistRadixTopK README,
+// "Distributed Radix Sort via NoC", first point: per-block histograms are
+// accumulated over the on-chip network, then prefix-summed).  Rank r reduces
+// slots [r*chunk, (r+1)*chunk) over every rank's `h_local` and broadcasts the
+// sums into every rank's merged histogram: a reduce-scatter followed by an
+// all-gather, both through distributed shared memory.  The caller must have
+// finished writing `h_local` (all threads reach the first cluster barrier).
+template <int NT, int C>
+__device__ void cluster_merge(const Smem& s, uint32_t* h_local, uint32_t rank, int tid) {
+    ptx::cluster_sync();
+    constexpr int chunk = kBinsX / C;
+    static_assert(chunk % 4 == 0, "merge chunk must be whole uint4s");
+    const uint32_t lbase = ptx::smem_addr(h_local) + rank * chunk * 4u;
+    const uint32_t mbase = ptx::smem_addr(s.hist_m) + rank * chunk * 4u;
+    for (int i = tid * 4; i < chunk; i += NT * 4) {
+        uint4 acc = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int q = 0; q < C; ++q) {
+            const uint4 v = ptx::ld_cluster_v4(ptx::map_rank(lbase + i * 4u, q));
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+#pragma unroll
+        for (int q = 0; q < C; ++q) ptx::st_cluster_v4(ptx::map_rank(mbase + i * 4u, q), acc);
+    }
+    ptx::cluster_sync();
+}
+
+// Position of gate sample i of a row of length L with M samples: every
+// position when the row is short, otherwise 32-wide contiguous segments (one
+// coalesced 128-byte read per warp) whose starts follow a golden-ratio
+// sequence, so that the segments do not alias with periodic score patterns.
+__device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t M) {
+    if (L <= M) return i;
+    const uint32_t seg = i >> 5;
+    const uint64_t frac = static_cast<uint64_t>(seg * 0x9E3779B9u);
+    const uint32_t start = static_cast<uint32_t>((frac * static_cast<uint64_t>(L - 31u)) >> 32) & ~3u;
+    return start + (i & 31u);
+}
+
+}  // namespace
+
+// ============================================================================
+// select_kernel<NT, C>: NT threads per block, C blocks per row (C == 1: one
+// block per row; C > 1: a thread-block cluster per row, each block owning a
+// contiguous slice of the row, rank order == position order).
+//
+// Per row:
+//  1. Gate.  Up to `samples` scores of the row are read (prefetched while the
+//     previous row is processed).  Their keys give a lower bound `lo` that
+//     about 2*k elements of the row exceed (the sample's r-th largest key,
+//     r = 2*E + 8 with E the expected number of samples in the top k) and a
+//     bin width so that the sampled range covers about 1024 of the 2048 bins
+//     (the "linear mapping" of the DistRadixTopK README: bins spread over the
+//     range where the threshold lies, so few elements share its bin).
+//  2. Pass 1 streams the slice through the bulk-copy ring: every element with
+//     key >= lo is counted in the histogram and pushed (key, position) into a
+//     candidate buffer in shared memory.  In a cluster the histograms are
+//     merged through distributed shared memory.
+//  3. Resolve.  Scanning the merged histogram from the top gives the bin of
+//     the k-th key; later 11-bit rounds histogram only the candidates inside
+//     that bin, until either the bin is a single key or it holds <= 32
+//     candidates, which a warp sort finishes (ties by smaller position).
+//     When the buffer overflowed (or the gate was too tight) the rounds
+//     re-read the slice from memory instead, and once the threshold bin fits
+//     a collect pass fills the buffer with it: the two-pass streaming path.
+//     A single threshold key tied by many elements takes the smallest
+//     positions: per-rank quotas in rank order, then a selection on position.
+//  4. Emit + transform.  Selected positions go to a shared-memory list; after
+//     a barrier the page-table gather writes out (and raw_out) coalesced,
+//     padding with -1 (PR #26788, commit "Dynamic dispatch via the plan's
+//     cluster_threshold": the transform is a separate pass).
+// ============================================================================
+template <int NT, int C>
+__global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const Layout lay = make_layout(C, p.tile, p.stages, p.cap, p.k);
+    Smem s;
+    s.ring = reinterpret_cast<float*>(smem_raw + lay.ring);
+    s.hist_a = reinterpret_cast<uint32_t*>(smem_raw + lay.hist_a);
+    s.hist_b = reinterpret_cast<uint32_t*>(smem_raw + lay.hist_b);
+    s.hist_m = reinterpret_cast<uint32_t*>(smem_raw + lay.hist_m);
+    s.cand_key = reinterpret_cast<uint32_t*>(smem_raw + lay.cand_key);
+    s.cand_idx = reinterpret_cast<uint32_t*>(smem_raw + lay.cand_idx);
+    s.emit = reinterpret_cast<uint32_t*>(smem_raw + lay.emit);
+    s.fin_key = reinterpret_cast<uint32_t*>(smem_raw + lay.fin_key);
+    s.fin_idx = reinterpret_cast<uint32_t*>(smem_raw + lay.fin_idx);
+    s.warp_tot = reinterpret_cast<uint32_t*>(smem_raw + lay.warp_tot);
+    s.ctl = reinterpret_cast<Control*>(smem_raw + lay.ctl);
+    s.it_row = reinterpret_cast<int32_t*>(smem_raw + lay.items_row);
+    s.it_len = reinterpret_cast<int32_t*>(smem_raw + lay.items_len);
+    s.full = reinterpret_cast<uint64_t*>(smem_raw + lay.mbar);
+    s.empty = s.full + p.stages;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = (C > 1) ? ptx::cluster_ctarank() : 0u;
+    const uint32_t unit = (C > 1) ? ptx::cluster_id_x() : blockIdx.x;
+    const uint32_t nunits = (C > 1) ? ptx::cluster_count_x() : gridDim.x;
+    if (p.plan && (p.plan->magic != kPlanMagic || p.plan->batch != p.batch ||
+                   p.plan->max_seq_len != p.max_seq_len)) {
+        if (tid == 0 && rank == 0 && unit == 0) atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
+        return;  // same for every block of a cluster
+    }
+    const int32_t n_first = min(p.n_items_dev ? *p.n_items_dev : p.n_items_host, p.batch);
+    const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
+    const int32_t n_items = n_first + max(n_second, 0);
+    const int32_t my_items = n_items > static_cast<int32_t>(unit)
+                                 ? (n_items - 1 - static_cast<int32_t>(unit)) / static_cast<int32_t>(nunits) + 1
+                                 : 0;
+    if (my_items <= 0) return;  // same for every block of a cluster
+
+    const uint32_t K = static_cast<uint32_t>(p.k);
+    const uint32_t cap = static_cast<uint32_t>(p.cap);
+    const uint32_t tile = static_cast<uint32_t>(p.tile);
+    const uint32_t stages = static_cast<uint32_t>(p.stages);
+
+    // ---------------------------------------------------------------- init
+    if (tid == 0) {
+        for (uint32_t i = 0; i < stages; ++i) {
+            ptx::mbar_init(&s.full[i], 1);
+            ptx::mbar_init(&s.empty[i], NT / 32);
+        }
+        ptx::fence_mbarrier_init();
+        Control* c = s.ctl;
+        c->ncand = c->nemit = c->nfin = c->smax = 0;
+        c->err = 0;
+    }
+    clear_hist<NT>(s.hist_a, tid);
+    clear_hist<NT>(s.hist_b, tid);
+    __syncthreads();
+    if (C > 1) ptx::cluster_sync();  // every block of the cluster is running before any DSMEM access
+
+    const uint64_t policy = ptx::l2_policy_evict_first();
+    const uint32_t m_max = static_cast<uint32_t>(p.samples);
+
+    // Producer state (meaningful in thread 0 only) and the consumer sequence.
+    uint32_t pseq = 0, cseq = 0;
+    int32_t p_item = 0;
+    uint32_t p_tile = 0;
+    bool aborted = false;
+
+    auto slice_of = [&](int32_t L, uint32_t& s0, uint32_t& s1) {
+        const uint32_t chunk = ((static_cast<uint32_t>(L) + C - 1) / C + 3u) & ~3u;
+        s0 = min(static_cast<uint32_t>(L), rank * chunk);
+        s1 = min(static_cast<uint32_t>(L), s0 + chunk);
+    };
+    auto tiles_of = [&](int32_t L) -> uint32_t {
+        if (L <= p.k) return 0u;
+        uint32_t s0, s1;
+        slice_of(L, s0, s1);
+        if (s1 <= s0) return 0u;
+        const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
+        return (n4 + tile - 1) / tile;
+    };
+
+    for (int32_t w0 = 0; w0 < my_items; w0 += kItemsMax) {
+        const int32_t nw = min(kItemsMax, my_items - w0);
+        for (int32_t i = tid; i < nw; i += NT) {
+            const int32_t it = static_cast<int32_t>(unit) + (w0 + i) * static_cast<int32_t>(nunits);
+            const int32_t row = it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first];
+            if (row < 0 || row >= p.batch) {  // a list that does not belong to this batch
+                atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
+                s.it_row[i] = 0;
+                s.it_len[i] = -1;
+                continue;
+            }
+            int32_t L = p.seq_lens[row];
+            if (L < 0) {
+                atomicOr(p.flags, TOPK_FLAG_SEQ_NEGATIVE);
+                L = 0;
+            } else if (L > p.max_seq_len) {
+                atomicOr(p.flags, TOPK_FLAG_SEQ_CLAMPED);
+                L = p.max_seq_len;
+            }
+            s.it_row[i] = row;
+            s.it_len[i] = L;
+        }
+        __syncthreads();
+        p_item = 0;
+        p_tile = 0;
+
+        // Thread 0 keeps the ring full: tiles up to `must` are issued even if
+        // that means waiting for a stage to drain; later ones only if a stage
+        // is already free.
+        auto pump = [&](uint32_t must) {
+            while (p_item < nw && pseq < cseq + stages && !aborted) {
+                const int32_t L = s.it_len[p_item];
+                const uint32_t nt = tiles_of(L);
+                if (nt == 0) {
+                    ++p_item;
+                    p_tile = 0;
+                    continue;
+                }
+                const uint32_t st = pseq % stages;
+                if (pseq >= stages) {
+                    const uint32_t par = ((pseq / stages) - 1u) & 1u;
+                    if (pseq <= must) {
+                        if (!ptx::mbar_wait_bounded(&s.empty[st], par, p.timeout_ns)) {
+                            aborted = true;
+                            atomicOr(&s.ctl->err, TOPK_FLAG_TIMEOUT);
+                            break;
+                        }
+                    } else if (!ptx::mbar_try_wait(&s.empty[st], par)) {
+                        break;
+                    }
+                }
+                uint32_t s0, s1;
+                slice_of(L, s0, s1);
+                const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
+                const uint32_t off = p_tile * tile;
+                const uint32_t elems = min(tile, n4 - off);
+                const float* src = p.scores + static_cast<int64_t>(s.it_row[p_item]) * p.row_stride + s0 + off;
+                ptx::mbar_arrive_expect_tx(&s.full[st], elems * 4u);
+                ptx::bulk_copy_g2s(s.ring + static_cast<size_t>(st) * tile, src, elems * 4u, &s.full[st], policy);
+                ++pseq;
+                if (++p_tile == nt) {
+                    ++p_item;
+                    p_tile = 0;
+                }
+            }
+        };
+
+        // Gate samples of the next non-trivial row are loaded one row ahead.
+        float smp[kSamplesPerThread];
+        auto load_samples = [&](int32_t j) {
+#pragma unroll
+            for (int q = 0; q < kSamplesPerThread; ++q) smp[q] = 0.0f;
+            if (j >= nw) return;
+            const int32_t L = s.it_len[j];
+            if (L <= p.k) return;
+            const uint32_t M = min(m_max, static_cast<uint32_t>(L));
+            const float* rowp = p.scores + static_cast<int64_t>(s.it_row[j]) * p.row_stride;
+#pragma unroll
+            for (int q = 0; q < kSamplesPerThread; ++q) {
+                const uint32_t i = static_cast<uint32_t>(q * NT + tid);
+                if (i < M) smp[q] = __ldg(rowp + sample_pos(i, static_cast<uint32_t>(L), M));
+            }
+        };
+        load_samples(0);
+
+        for (int32_t j = 0; j < nw; ++j) {
+            const int32_t row = s.it_row[j];
+            const int32_t L = s.it_len[j];
+            if (L < 0) {  // rejected item: nothing to write
+                load_samples(j + 1);
+                continue;
+            }
+            const uint32_t Kp = min(K, static_cast<uint32_t>(L));
+            int32_t* out_row = p.out + static_cast<int64_t>(row) * p.k;
+            int32_t* raw_row = p.raw_out ? p.raw_out + static_cast<int64_t>(row) * p.k : nullptr;
+            const int32_t* pt_row = p.page_table + static_cast<int64_t>(row) * p.pt_stride;
+
+            if (static_cast<uint32_t>(L) <= K) {
+                // Every position is selected (seq_len <= k): no select at all.
+                if (rank == 0) {
+                    for (uint32_t q = tid; q < K; q += NT) {
+                        const int32_t r = q < static_cast<uint32_t>(L) ? static_cast<int32_t>(q) : -1;
+                        out_row[q] = page_map(pt_row, p.log2_page, r);
+                        if (raw_row) raw_row[q] = r;
+                    }
+                }
+                load_samples(j + 1);
+                continue;
+            }
+
+            uint32_t s0, s1;
+            slice_of(L, s0, s1);
+            const uint32_t ntiles = tiles_of(L);
+            const float* row_ptr = p.scores + static_cast<int64_t>(row) * p.row_stride;
+
+            if (tid == 0) {
+                s.ctl->ncand = 0;
+                s.ctl->nemit = 0;
+                s.ctl->nfin = 0;
+                s.ctl->smax = 0;
+            }
+            __syncthreads();
+
+            // ------------------------------------------------------ 1. gate
+            uint32_t lo = 0;
+            int shift = 32 - kBinBits;
+            {
+                const uint32_t M = min(m_max, static_cast<uint32_t>(L));
+                const uint64_t r64 =
+                    (2ull * M * Kp + static_cast<uint64_t>(L) - 1ull) / static_cast<uint64_t>(L) + 8ull;
+                if (!p.disable_gate && r64 < M) {
+                    const uint32_t r = static_cast<uint32_t>(r64);
+                    uint32_t keys[kSamplesPerThread];
+                    uint32_t kmax = 0;
+#pragma unroll
+                    for (int q = 0; q < kSamplesPerThread; ++q) {
+                        const uint32_t i = static_cast<uint32_t>(q * NT + tid);
+                        keys[q] = score_key(smp[q]);
+                        if (i < M) {
+                            atomicAdd(&s.hist_a[keys[q] >> (32 - kBinBits)], 1u);
+                            kmax = max(kmax, keys[q]);
+                        }
+                    }
+                    kmax = __reduce_max_sync(kFull, kmax);
+                    if (lane == 0) atomicMax(&s.ctl->smax, kmax);
+                    __syncthreads();
+                    const ScanResult g = scan_find<NT>(s, s.hist_a, r, tid);
+                    lo = g.bin << (32 - kBinBits);
+                    if (g.above + g.count > 2u * r && g.count > 1u) {
+                        // Refine inside the coarse bin on the next 11 bits.
+#pragma unroll
+                        for (int q = 0; q < kSamplesPerThread; ++q) {
+                            const uint32_t i = static_cast<uint32_t>(q * NT + tid);
+                            if (i < M && (keys[q] >> (32 - kBinBits)) == g.bin)
+                                atomicAdd(&s.hist_b[(keys[q] >> (32 - 2 * kBinBits)) & (kBins - 1)], 1u);
+                        }
+                        __syncthreads();
+                        const ScanResult g2 = scan_find<NT>(s, s.hist_b, r - g.above, tid);
+                        lo |= g2.bin << (32 - 2 * kBinBits);
+                        clear_hist<NT>(s.hist_b, tid);
+                    }
+                    clear_hist<NT>(s.hist_a, tid);
+                    const uint32_t smax = s.ctl->smax;
+                    const int b = bit_length(smax - lo);
+                    shift = b > kBinBits - 1 ? b - (kBinBits - 1) : 0;
+                    __syncthreads();
+                }
+            }
+            load_samples(j + 1);
+
+            // ------------------------------------------------- 2. pass 1
+            const bool buffering = !p.force_two_pass;
+            for (uint32_t t = 0; t < ntiles; ++t) {
+                if (tid == 0) pump(cseq);
+                __syncwarp();
+                const uint32_t st = cseq % stages;
+                const bool gave_up = (*reinterpret_cast<volatile uint32_t*>(&s.ctl->err) & TOPK_FLAG_TIMEOUT) != 0u;
+                if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns)) {
+                    atomicOr(&s.ctl->err, TOPK_FLAG_TIMEOUT);
+                    aborted = true;
+                }
+                const uint32_t off = t * tile;
+                const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
+                const uint32_t nvec = min(tile, n4 - off) >> 2;
+                const float4* v4 = reinterpret_cast<const float4*>(s.ring + static_cast<size_t>(st) * tile);
+                const uint32_t base_idx = s0 + off;
+                for (uint32_t v = tid; v < nvec; v += NT) {
+                    const float4 x = v4[v];
+                    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t idx = base_idx + 4u * v + c;
+                        const uint32_t key = score_key(xs[c]);
+                        if (key >= lo && idx < s1) {
+                            const uint32_t bin = min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1));
+                            atomicAdd(&s.hist_a[bin], 1u);
+                            if (buffering) {
+                                const uint32_t slot = atomicAdd(&s.ctl->ncand, 1u);
+                                if (slot < cap) {
+                                    s.cand_key[slot] = key;
+                                    s.cand_idx[slot] = idx;
+                                }
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&s.empty[st]);
+                ++cseq;
+            }
+            __syncthreads();
+            if (tid == 0) pump(0);  // prefetch the next row while this one resolves
+
+            const uint32_t local_ovf = (!buffering || s.ctl->ncand > cap) ? 1u : 0u;
+            const uint32_t* hm = s.hist_a;
+            if (C > 1) {
+                if (tid == 0) s.hist_a[kSlotOverflow] = local_ovf;
+                cluster_merge<NT, C>(s, s.hist_a, rank, tid);
+                hm = s.hist_m;
+            }
+            const bool overflow = (C > 1) ? (hm[kSlotOverflow] != 0u) : (local_ovf != 0u);
+            ScanResult sr = scan_find<NT>(s, hm, Kp, tid);
+
+            // ----------------------------------------------------- 3. resolve
+            uint32_t r_lo, r_hi, G, cnt, local_cnt = 0;
+            bool stream_mode;
+            if (sr.total < Kp || sr.bin >= static_cast<uint32_t>(kBins)) {
+                // The gate was tighter than the k-th key: recount everything.
+                r_lo = 0;
+                r_hi = 0xffffffffu;
+                G = 0;
+                cnt = 0xffffffffu;
+                stream_mode = true;
+            } else {
+                G = sr.above;
+                const uint64_t b = sr.bin;
+                r_lo = static_cast<uint32_t>(lo + (b << shift));
+                r_hi = (sr.bin == kBins - 1)
+                           ? 0xffffffffu
+                           : static_cast<uint32_t>(min_u64(0xffffffffull, lo + ((b + 1) << shift) - 1));
+                cnt = sr.count;
+                stream_mode = overflow;
+                local_cnt = s.hist_a[sr.bin];
+            }
+            clear_hist<NT>(s.hist_a, tid);
+            uint32_t* h_next = s.hist_b;
+            uint32_t* h_other = s.hist_a;
+
+            const uint32_t n4_slice = (s1 > s0) ? ((s1 + 3u) & ~3u) - s0 : 0u;
+            const uint32_t nvec_slice = n4_slice >> 2;
+            const float4* slice4 = reinterpret_cast<const float4*>(row_ptr + s0);
+
+            auto emit_push = [&](uint32_t idx) {
+                const uint32_t slot = atomicAdd(&s.ctl->nemit, 1u);
+                if (slot < K)
+                    s.emit[slot] = idx;
+                else
+                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+            };
+
+            for (int round = 0;; ++round) {
+                if (round > 8) {
+                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                    break;
+                }
+                if (r_lo == r_hi) break;
+                if (!stream_mode && cnt <= static_cast<uint32_t>(kFinish)) break;
+                if (stream_mode && cnt <= cap) {
+                    // Collect pass: emit everything above the bin, keep the bin.
+                    __syncthreads();
+                    if (tid == 0) s.ctl->ncand = 0;
+                    __syncthreads();
+                    for (uint32_t v = tid; v < nvec_slice; v += NT) {
+                        const float4 x = __ldg(slice4 + v);
+                        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t idx = s0 + 4u * v + c;
+                            const uint32_t key = score_key(xs[c]);
+                            if (idx < s1 && key >= r_lo) {
+                                if (key > r_hi) {
+                                    emit_push(idx);
+                                } else {
+                                    const uint32_t slot = atomicAdd(&s.ctl->ncand, 1u);
+                                    if (slot < cap) {
+                                        s.cand_key[slot] = key;
+                                        s.cand_idx[slot] = idx;
+                                    } else {
+                                        atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    __syncthreads();
+                    stream_mode = false;
+                    continue;
+                }
+                // One more 11-bit round over [r_lo, r_hi].
+                const int sh = shift_for_span(r_hi - r_lo);
+                if (!stream_mode) {
+                    const uint32_t nc = s.ctl->ncand;
+                    for (uint32_t i = tid; i < nc; i += NT) {
+                        const uint32_t key = s.cand_key[i];
+                        if (key >= r_lo && key <= r_hi) atomicAdd(&h_next[(key - r_lo) >> sh], 1u);
+                    }
+                } else {
+                    for (uint32_t v = tid; v < nvec_slice; v += NT) {
+                        const float4 x = __ldg(slice4 + v);
+                        const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t idx = s0 + 4u * v + c;
+                            const uint32_t key = score_key(xs[c]);
+                            if (idx < s1 && key >= r_lo && key <= r_hi) atomicAdd(&h_next[(key - r_lo) >> sh], 1u);
+                        }
+                    }
+                }
+                __syncthreads();
+                const uint32_t* hr = h_next;
+                if (C > 1) {
+                    cluster_merge<NT, C>(s, h_next, rank, tid);
+                    hr = s.hist_m;
+                }
+                sr = scan_find<NT>(s, hr, Kp - G, tid);
+                if (sr.bin >= static_cast<uint32_t>(kBins)) {  // cannot happen: the bin holds >= need
+                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                    clear_hist<NT>(h_next, tid);
+                    break;
+                }
+                local_cnt = h_next[sr.bin];
+                G += sr.above;
+                const uint64_t b = sr.bin;
+                const uint32_t nlo = static_cast<uint32_t>(r_lo + (b << sh));
+                const uint32_t nhi = static_cast<uint32_t>(min_u64(r_hi, r_lo + ((b + 1) << sh) - 1));
+                r_lo = nlo;
+                r_hi = nhi;
+                cnt = sr.count;
+                clear_hist<NT>(h_next, tid);
+                uint32_t* t = h_next;
+                h_next = h_other;
+                h_other = t;
+            }
+            __syncthreads();
+
+            const uint32_t need = Kp - G;
+            if (r_lo == r_hi) {
+                // ---- a single threshold key T; `need` of its `cnt` copies are taken
+                const uint32_t T = r_lo;
+                uint32_t quota = need;
+                if (C > 1) {
+                    if (tid < C) ptx::st_cluster_u32(ptx::map_rank(ptx::smem_addr(&s.ctl->rank_eq[rank]), tid),
+                                                     local_cnt);
+                    ptx::cluster_sync();
+                    uint32_t before = 0;
+                    for (uint32_t q = 0; q < rank; ++q) before += s.ctl->rank_eq[q];
+                    quota = need > before ? min(need - before, local_cnt) : 0u;
+                }
+                const bool all_eq = (quota == local_cnt);
+                if (!stream_mode) {
+                    const uint32_t nc = s.ctl->ncand;
+                    for (uint32_t i = tid; i < nc; i += NT) {
+                        const uint32_t key = s.cand_key[i];
+                        if (key > T || (all_eq && key == T)) emit_push(s.cand_idx[i]);
+                    }
+                    if (!all_eq && quota > 0) {
+                        // The `quota` smallest positions among this block's copies of T:
+                        // rounds on v = ~position (larger v = smaller position).
+                        uint32_t v_lo = ~(s1 - 1u), v_hi = ~s0, v_g = 0, v_cnt = local_cnt;
+                        for (int vr = 0; vr < 6; ++vr) {
+                            if (v_lo == v_hi || v_cnt <= static_cast<uint32_t>(kFinish)) break;
+                            const int sh = shift_for_span(v_hi - v_lo);
+                            for (uint32_t i = tid; i < nc; i += NT) {
+                                const uint32_t v = ~s.cand_idx[i];
+                                if (s.cand_key[i] == T && v >= v_lo && v <= v_hi)
+                                    atomicAdd(&h_next[(v - v_lo) >> sh], 1u);
+                            }
+                            __syncthreads();
+                            const ScanResult vs = scan_find<NT>(s, h_next, quota - v_g, tid);
+                            v_g += vs.above;
+                            const uint64_t b = vs.bin;
+                            const uint32_t nlo = static_cast<uint32_t>(v_lo + (b << sh));
+                            const uint32_t nhi = static_cast<uint32_t>(min_u64(v_hi, v_lo + ((b + 1) << sh) - 1));
+                            v_lo = nlo;
+                            v_hi = nhi;
+                            v_cnt = vs.count;
+                            clear_hist<NT>(h_next, tid);
+                            __syncthreads();
+                        }
+                        // Above the final range: taken.  Inside it: a warp sort picks the rest.
+                        if (tid == 0) s.ctl->nfin = 0;
+                        __syncthreads();
+                        for (uint32_t i = tid; i < nc; i += NT) {
+                            if (s.cand_key[i] != T) continue;
+                            const uint32_t v = ~s.cand_idx[i];
+                            if (v > v_hi) {
+                                emit_push(s.cand_idx[i]);
+                            } else if (v >= v_lo) {
+                                const uint32_t slot = atomicAdd(&s.ctl->nfin, 1u);
+                                if (slot < static_cast<uint32_t>(kFinish)) {
+                                    s.fin_key[slot] = v;
+                                    s.fin_idx[slot] = s.cand_idx[i];
+                                } else {
+                                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                }
+                            }
+                        }
+                        __syncthreads();
+                        if (warp == 0) {
+                            const uint32_t nf = min(s.ctl->nfin, static_cast<uint32_t>(kFinish));
+                            const uint64_t e = lane < static_cast<int>(nf)
+                                                   ? (static_cast<uint64_t>(s.fin_key[lane]) << 32) | 1ull
+                                                   : 0ull;
+                            const uint64_t srt = warp_sort_desc(e, lane);
+                            const uint32_t take = quota - v_g;
+                            if (static_cast<uint32_t>(lane) < take && srt != 0ull)
+                                emit_push(~static_cast<uint32_t>(srt >> 32));
+                        }
+                    }
+                } else {
+                    // Final streaming pass: > T is taken; copies of T up to the quota,
+                    // in position order when only some of them are taken.
+                    const bool ordered = (!all_eq && quota > 0);
+                    uint32_t running = 0;
+                    for (uint32_t vb = 0; vb < nvec_slice; vb += NT) {
+                        const uint32_t v = vb + tid;
+                        uint32_t eqm = 0;
+                        if (v < nvec_slice) {
+                            const float4 x = __ldg(slice4 + v);
+                            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t idx = s0 + 4u * v + c;
+                                const uint32_t key = score_key(xs[c]);
+                                if (idx < s1) {
+                                    if (key > T)
+                                        emit_push(idx);
+                                    else if (key == T)
+                                        eqm |= 1u << c;
+                                }
+                            }
+                        }
+                        if (!ordered) {
+                            if (all_eq)
+                                for (int c = 0; c < 4; ++c)
+                                    if (eqm >> c & 1u) emit_push(s0 + 4u * v + c);
+                            continue;
+                        }
+                        const uint32_t n_eq = __popc(eqm);
+                        const uint32_t incl = warp_inclusive_sum(n_eq, lane);
+                        if (lane == 31) s.warp_tot[warp] = incl;
+                        __syncthreads();
+                        uint32_t pre = 0, tot = 0;
+                        for (int w = 0; w < NT / 32; ++w) {
+                            const uint32_t t = s.warp_tot[w];
+                            pre += (w < warp) ? t : 0u;
+                            tot += t;
+                        }
+                        uint32_t r0 = running + pre + incl - n_eq;
+                        for (int c = 0; c < 4; ++c) {
+                            if (eqm >> c & 1u) {
+                                if (r0 < quota) emit_push(s0 + 4u * v + c);
+                                ++r0;
+                            }
+                        }
+                        running += tot;
+                        __syncthreads();
+                    }
+                }
+            } else {
+                // ---- <= 32 candidates in [r_lo, r_hi]: warp compare-and-swap finish
+                const uint32_t nc = s.ctl->ncand;
+                const uint32_t fin_nfin = ptx::smem_addr(&s.ctl->nfin);
+                const uint32_t fin_key0 = ptx::smem_addr(s.fin_key);
+                const uint32_t fin_idx0 = ptx::smem_addr(s.fin_idx);
+                for (uint32_t i = tid; i < nc; i += NT) {
+                    const uint32_t key = s.cand_key[i];
+                    if (key > r_hi) {
+                        emit_push(s.cand_idx[i]);
+                    } else if (key >= r_lo) {
+                        if (C > 1) {
+                            const uint32_t slot = ptx::atom_add_cluster_u32(ptx::map_rank(fin_nfin, 0), 1u);
+                            if (slot < static_cast<uint32_t>(kFinish)) {
+                                ptx::st_cluster_u32(ptx::map_rank(fin_key0 + slot * 4u, 0), key);
+                                ptx::st_cluster_u32(ptx::map_rank(fin_idx0 + slot * 4u, 0), s.cand_idx[i]);
+                            } else {
+                                atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                            }
+                        } else {
+                            const uint32_t slot = atomicAdd(&s.ctl->nfin, 1u);
+                            if (slot < static_cast<uint32_t>(kFinish)) {
+                                s.fin_key[slot] = key;
+                                s.fin_idx[slot] = s.cand_idx[i];
+                            } else {
+                                atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                            }
+                        }
+                    }
+                }
+                if (C > 1)
+                    ptx::cluster_sync();
+                else
+                    __syncthreads();
+                if (rank == 0 && warp == 0) {
+                    const uint32_t nf = min(s.ctl->nfin, static_cast<uint32_t>(kFinish));
+                    const uint64_t e = lane < static_cast<int>(nf)
+                                           ? (static_cast<uint64_t>(s.fin_key[lane]) << 32) | (~s.fin_idx[lane])
+                                           : 0ull;
+                    const uint64_t srt = warp_sort_desc(e, lane);
+                    if (static_cast<uint32_t>(lane) < need && srt != 0ull)
+                        emit_push(~static_cast<uint32_t>(srt & 0xffffffffull));
+                }
+            }
+            __syncthreads();
+
+            // ------------------------------------------- 4. transform + write
+            const uint32_t nemit = min(s.ctl->nemit, K);
+            if (C == 1) {
+                if (nemit != Kp && tid == 0) atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                for (uint32_t q = tid; q < K; q += NT) {
+                    const int32_t r = q < nemit ? static_cast<int32_t>(s.emit[q]) : -1;
+                    out_row[q] = page_map(pt_row, p.log2_page, r);
+                    if (raw_row) raw_row[q] = r;
+                }
+            } else {
+                if (tid < C)
+                    ptx::st_cluster_u32(ptx::map_rank(ptx::smem_addr(&s.ctl->rank_cnt[rank]), tid), nemit);
+                ptx::cluster_sync();
+                uint32_t before = 0, total = 0;
+                for (uint32_t q = 0; q < static_cast<uint32_t>(C); ++q) {
+                    const uint32_t c = s.ctl->rank_cnt[q];
+                    before += (q < rank) ? c : 0u;
+                    total += c;
+                }
+                if (rank == 0 && tid == 0 && total != Kp) atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                for (uint32_t q = tid; q < nemit; q += NT) {
+                    const uint32_t slot = before + q;
+                    if (slot < K) {
+                        const int32_t r = static_cast<int32_t>(s.emit[q]);
+                        out_row[slot] = page_map(pt_row, p.log2_page, r);
+                        if (raw_row) raw_row[slot] = r;
+                    }
+                }
+                if (rank == 0) {
+                    for (uint32_t q = total + tid; q < K; q += NT) {
+                        out_row[q] = -1;
+                        if (raw_row) raw_row[q] = -1;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        __syncthreads();
+    }
+
+    // Drain: nothing may still be copying into this block's shared memory.
+    if (tid == 0) {
+        while (pseq > cseq) {
+            const uint32_t st = cseq % stages;
+            if (!ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns)) break;
+            ++cseq;
+        }
+        if (s.ctl->err) atomicOr(p.flags, s.ctl->err);
+    }
+    if (C > 1) ptx::cluster_sync();  // no block leaves while others may still address its shared memory
+}
+
+namespace {
+
+__device__ __forceinline__ int length_bucket(int32_t L) {
+    if (L <= 0) return 0;
+    const int bl = bit_length(static_cast<uint32_t>(L));
+    if (bl < 2) return 2 * bl;
+    return 2 * bl + ((L >> (bl - 2)) & 1);
+}
+
+// Plan (PR #26788, commit "Replace the per-element cluster launch ...": the
+// plan compacts the long items into a work list).  One block: every row is
+// classified long (clamped seq_len > threshold) or short, and each class is
+// written as a list ordered by half-octave length bucket, longest first, so
+// that the persistent kernels hand out the longest rows first.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                                    int32_t threshold, void* ws) {
+    __shared__ uint32_t cnt[2][64];
+    __shared__ uint32_t cur[2][64];
+    __shared__ uint32_t flags;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < 128; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    if (tid == 0) flags = 0;
+    __syncthreads();
+    for (int32_t b = tid; b < batch; b += blockDim.x) {
+        int32_t L = seq_lens[b];
+        if (L < 0) {
+            atomicOr(&flags, TOPK_FLAG_SEQ_NEGATIVE);
+            L = 0;
+        } else if (L > max_seq_len) {
+            atomicOr(&flags, TOPK_FLAG_SEQ_CLAMPED);
+            L = max_seq_len;
+        }
+        atomicAdd(&cnt[L > threshold ? 1 : 0][length_bucket(L)], 1u);
+    }
+    __syncthreads();
+    if (tid < 2) {
+        uint32_t run = 0;
+        for (int k = 63; k >= 0; --k) {
+            cur[tid][k] = run;
+            run += cnt[tid][k];
+        }
+        cnt[tid][0] = run;  // total of the class (bucket 0 no longer needed)
+    }
+    __syncthreads();
+    int32_t* lists[2] = {plan_short_list(ws, batch), plan_long_list(ws)};
+    for (int32_t b = tid; b < batch; b += blockDim.x) {
+        int32_t L = seq_lens[b];
+        L = L < 0 ? 0 : (L > max_seq_len ? max_seq_len : L);
+        const int cls = L > threshold ? 1 : 0;
+        const uint32_t pos = atomicAdd(&cur[cls][length_bucket(L)], 1u);
+        lists[cls][pos] = b;
+    }
+    if (tid == 0) {
+        PlanHeader* h = static_cast<PlanHeader*>(ws);
+        h->magic = kPlanMagic;
+        h->batch = batch;
+        h->max_seq_len = max_seq_len;
+        h->long_threshold = threshold;
+        h->n_long = static_cast<int32_t>(cnt[1][0]);
+        h->n_short = static_cast<int32_t>(cnt[0][0]);
+        h->flags = flags;
+    }
+}
+
+__global__ void page_transform_kernel(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
+                                      int64_t pt_stride, int32_t log2_page, int32_t* out) {
+    const int64_t n = static_cast<int64_t>(batch) * k;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = i / k;
+        out[i] = page_map(page_table + b * pt_stride, log2_page, raw[i]);
+    }
+}
+
+__global__ void key_map_kernel(const float* x, int64_t n, uint32_t* keys) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        keys[i] = score_key(x[i]);
+}
+
+template <int NT, int C>
+cudaError_t launch_select_t(const SelectParams& p, int grid_units, size_t smem, cudaStream_t stream) {
+    auto kern = select_kernel<NT, C>;
+    static size_t smem_set = 0;
+    if (smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        if (C > 8) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        smem_set = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_units * C));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (C > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int NT, int C>
+cudaError_t occupancy_t(size_t smem, int* units) {
+    auto kern = select_kernel<NT, C>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (C == 1) {
+        int per_sm = 0, dev = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, smem);
+        if (e != cudaSuccess) return e;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        *units = per_sm * sms;
+        return cudaSuccess;
+    }
+    if (C > 8) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * 64);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    *units = clusters;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int select_threads(int cluster) { return cluster == 1 ? 256 : 512; }
+
+cudaError_t launch_select(const SelectParams& p, int cluster, int grid_units, size_t smem, cudaStream_t stream) {
+    switch (cluster) {
+        case 1: return launch_select_t<256, 1>(p, grid_units, smem, stream);
+        case 2: return launch_select_t<512, 2>(p, grid_units, smem, stream);
+        case 4: return launch_select_t<512, 4>(p, grid_units, smem, stream);
+        case 8: return launch_select_t<512, 8>(p, grid_units, smem, stream);
+        case 16: return launch_select_t<512, 16>(p, grid_units, smem, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t select_occupancy(int cluster, size_t smem, int* units_out) {
+    switch (cluster) {
+        case 1: return occupancy_t<256, 1>(smem, units_out);
+        case 2: return occupancy_t<512, 2>(smem, units_out);
+        case 4: return occupancy_t<512, 4>(smem, units_out);
+        case 8: return occupancy_t<512, 8>(smem, units_out);
+        case 16: return occupancy_t<512, 16>(smem, units_out);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
+                        void* workspace, cudaStream_t stream) {
+    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, batch, max_seq_len, long_threshold, workspace);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
+                                  int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream) {
+    const int64_t n = static_cast<int64_t>(batch) * k;
+    const int blocks = static_cast<int>(min_i64((n + 255) / 256, 152 * 8));
+    page_transform_kernel<<<blocks, 256, 0, stream>>>(raw, batch, k, page_table, pt_stride, log2_page, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const int blocks = static_cast<int>(min_i64((n + 255) / 256, 152 * 16));
+    key_map_kernel<<<blocks, 256, 0, stream>>>(x, n, keys);
+    return cudaGetLastError();
+}
+
+}  // namespace topkidx

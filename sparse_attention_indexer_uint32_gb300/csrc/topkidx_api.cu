@@ -1,0 +1,291 @@
+// topkidx_api.cu -- the C ABI declared in include/topkidx.h: argument checks,
+// the path split chosen by the plan, launch sizing and error mapping.  All
+// compute runs in the kernels of topk_kernels.cu; there is no host fallback.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "topk_internal.h"
+#include "topkidx.h"
+
+using namespace topkidx;
+
+namespace {
+
+std::mutex g_mutex;
+
+// Thresholds after SGLang PR #26788 (commit "Fuse the cluster/non-cluster
+// split for small batch": long rows above 32K for small batches, 64K
+// otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
+// PR).  Blocks per long row: 8, the cluster size both the PR and the
+// DistRadixTopK README use.
+topk_tuning_t g_tuning = {32768, 65536, 15, 8, 0, 0, 0, 0};
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int log2_exact(int64_t x) {
+    int r = 0;
+    while ((int64_t{1} << r) < x) ++r;
+    return r;
+}
+
+topk_status_t check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ECUDA;
+    static std::map<int, topk_status_t> known;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = known.find(dev);
+    if (it != known.end()) return it->second;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return TOPK_ECUDA;
+    const topk_status_t st = (major == 10 && minor == 3) ? TOPK_OK : TOPK_EDEVICE;
+    known[dev] = st;
+    return st;
+}
+
+int32_t long_threshold(const topk_tuning_t& t, int32_t batch) {
+    return batch <= t.small_batch_max ? t.long_threshold_small_batch : t.long_threshold;
+}
+
+struct PathConfig {
+    int cluster;
+    int tile;
+    int stages;
+    int cap;
+    int samples;
+    size_t smem;
+};
+
+PathConfig path_config(int cluster, int32_t k, const topk_tuning_t& t) {
+    PathConfig c;
+    c.cluster = cluster;
+    const int nt = select_threads(cluster);
+    if (cluster == 1) {
+        c.tile = 2048;
+        c.stages = 4;
+    } else {
+        c.tile = 2048;
+        c.stages = 4;
+    }
+    int cap = t.candidate_capacity;
+    if (cap == 0) {
+        cap = cluster == 1 ? 4 * k : 2 * k;
+        if (cap < 2048) cap = 2048;
+        if (cap > 16384) cap = 16384;
+        cap = (cap + 63) / 64 * 64;
+    }
+    c.cap = cap;
+    int samples = t.samples;
+    if (samples == 0) samples = kSamplesPerThread * nt;
+    if (samples > kSamplesPerThread * nt) samples = kSamplesPerThread * nt;
+    c.samples = samples;
+    c.smem = make_layout(cluster, c.tile, c.stages, c.cap, k).total;
+    return c;
+}
+
+// Resident units (blocks, or clusters) of the select kernel for a launch shape.
+topk_status_t resident_units(int cluster, size_t smem, int* units) {
+    static std::map<std::pair<int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(cluster * 64 + dev, smem);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *units = it->second;
+            return TOPK_OK;
+        }
+    }
+    int u = 0;
+    if (select_occupancy(cluster, smem, &u) != cudaSuccess || u <= 0) return TOPK_ECUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    cache[key] = u;
+    *units = u;
+    return TOPK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t topk_plan_workspace_bytes(int32_t batch) { return plan_bytes(batch); }
+
+const char* topk_status_string(topk_status_t status) {
+    switch (status) {
+        case TOPK_OK: return "ok";
+        case TOPK_EINVAL: return "invalid argument";
+        case TOPK_EALIGN: return "misaligned pointer or stride";
+        case TOPK_ECUDA: return "CUDA error";
+        case TOPK_ENOSPACE: return "workspace too small";
+        case TOPK_EDEVICE: return "device is not an sm_103 GPU";
+    }
+    return "unknown status";
+}
+
+topk_status_t topk_get_tuning(topk_tuning_t* tuning_host) {
+    if (!tuning_host) return TOPK_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    *tuning_host = g_tuning;
+    return TOPK_OK;
+}
+
+topk_status_t topk_set_tuning(const topk_tuning_t* t) {
+    if (!t) return TOPK_EINVAL;
+    if (t->long_threshold_small_batch < 0 || t->long_threshold < 0 || t->small_batch_max < 0) return TOPK_EINVAL;
+    if (t->cluster_size != 2 && t->cluster_size != 4 && t->cluster_size != 8 && t->cluster_size != 16)
+        return TOPK_EINVAL;
+    if (t->candidate_capacity != 0 &&
+        (t->candidate_capacity < 2048 || t->candidate_capacity > 16384 || t->candidate_capacity % 64 != 0))
+        return TOPK_EINVAL;
+    if (t->samples != 0 && (t->samples < 32 || t->samples > 4096 || t->samples % 32 != 0)) return TOPK_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_tuning = *t;
+    return TOPK_OK;
+}
+
+topk_status_t topk_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, void* workspace,
+                        size_t workspace_bytes, topk_stream_t stream) {
+    if (!seq_lens || !workspace || batch < 1 || max_seq_len < 0) return TOPK_EINVAL;
+    if (workspace_bytes < plan_bytes(batch)) return TOPK_ENOSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0 || reinterpret_cast<uintptr_t>(seq_lens) % 4 != 0)
+        return TOPK_EALIGN;
+    const topk_status_t dev = check_device();
+    if (dev != TOPK_OK) return dev;
+    topk_tuning_t t;
+    topk_get_tuning(&t);
+    if (launch_plan(seq_lens, batch, max_seq_len, long_threshold(t, batch), workspace,
+                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TOPK_ECUDA;
+    return TOPK_OK;
+}
+
+topk_status_t topk_transform(const float* scores, int64_t row_stride, const int32_t* seq_lens, int32_t batch,
+                             int32_t max_seq_len, const int32_t* page_table, int64_t page_table_stride,
+                             int32_t page_size, int32_t k, int32_t* out_indices, int32_t* out_raw_indices_or_null,
+                             void* workspace, topk_stream_t stream) {
+    if (!scores || !seq_lens || !page_table || !out_indices || !workspace) return TOPK_EINVAL;
+    if (batch < 1 || max_seq_len < 0 || k < 1 || k > kMaxK) return TOPK_EINVAL;
+    if (!is_pow2(page_size) || page_size > (1 << 30)) return TOPK_EINVAL;
+    if (row_stride < max_seq_len || row_stride < 1) return TOPK_EINVAL;
+    if (page_table_stride < (static_cast<int64_t>(max_seq_len) + page_size - 1) / page_size || page_table_stride < 1)
+        return TOPK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(scores) % 16 != 0 || row_stride % 4 != 0) return TOPK_EALIGN;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return TOPK_EALIGN;
+    if (reinterpret_cast<uintptr_t>(seq_lens) % 4 || reinterpret_cast<uintptr_t>(page_table) % 4 ||
+        reinterpret_cast<uintptr_t>(out_indices) % 4 || reinterpret_cast<uintptr_t>(out_raw_indices_or_null) % 4)
+        return TOPK_EALIGN;
+    const topk_status_t dev = check_device();
+    if (dev != TOPK_OK) return dev;
+
+    topk_tuning_t t;
+    topk_get_tuning(&t);
+    const int32_t threshold = long_threshold(t, batch);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    auto* hdr = static_cast<PlanHeader*>(workspace);
+
+    SelectParams p = {};
+    p.scores = scores;
+    p.row_stride = row_stride;
+    p.seq_lens = seq_lens;
+    p.batch = batch;
+    p.max_seq_len = max_seq_len;
+    p.page_table = page_table;
+    p.pt_stride = page_table_stride;
+    p.log2_page = log2_exact(page_size);
+    p.k = k;
+    p.out = out_indices;
+    p.raw_out = out_raw_indices_or_null;
+    p.plan = hdr;
+    p.flags = &hdr->flags;
+    p.force_two_pass = t.force_two_pass;
+    p.disable_gate = t.disable_gate;
+    p.timeout_ns = 2000000000ull;
+
+    const bool launch_long = max_seq_len > threshold;
+    if (launch_long) {
+        const PathConfig c = path_config(t.cluster_size, k, t);
+        int units = 0;
+        const topk_status_t r = resident_units(c.cluster, c.smem, &units);
+        if (r != TOPK_OK) return r;
+        SelectParams q = p;
+        q.items = plan_long_list(workspace);
+        q.n_items_dev = &hdr->n_long;
+        q.tile = c.tile;
+        q.stages = c.stages;
+        q.cap = c.cap;
+        q.samples = c.samples;
+        const int grid = batch < units ? batch : units;
+        if (launch_select(q, c.cluster, grid, c.smem, st) != cudaSuccess) return TOPK_ECUDA;
+    }
+    {
+        const PathConfig c = path_config(1, k, t);
+        int units = 0;
+        const topk_status_t r = resident_units(1, c.smem, &units);
+        if (r != TOPK_OK) return r;
+        SelectParams q = p;
+        q.items = plan_short_list(workspace, batch);
+        q.n_items_dev = &hdr->n_short;
+        if (!launch_long) {  // rows the plan called long (if any) are taken here too
+            q.items2 = plan_long_list(workspace);
+            q.n_items2_dev = &hdr->n_long;
+        }
+        q.tile = c.tile;
+        q.stages = c.stages;
+        q.cap = c.cap;
+        q.samples = c.samples;
+        // Equal shares: the fewest blocks that still give every block the
+        // same number of rows when all rows are short.
+        const int per_unit = (batch + units - 1) / units;
+        const int grid = (batch + per_unit - 1) / per_unit;
+        if (launch_select(q, 1, grid, c.smem, st) != cudaSuccess) return TOPK_ECUDA;
+    }
+    return TOPK_OK;
+}
+
+topk_status_t topk_page_transform(const int32_t* raw_indices, int32_t batch, int32_t k, const int32_t* page_table,
+                                  int64_t page_table_stride, int32_t page_size, int32_t* out_indices,
+                                  topk_stream_t stream) {
+    if (!raw_indices || !page_table || !out_indices || batch < 1 || k < 1 || page_table_stride < 1)
+        return TOPK_EINVAL;
+    if (!is_pow2(page_size) || page_size > (1 << 30)) return TOPK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(raw_indices) % 4 || reinterpret_cast<uintptr_t>(page_table) % 4 ||
+        reinterpret_cast<uintptr_t>(out_indices) % 4)
+        return TOPK_EALIGN;
+    const topk_status_t dev = check_device();
+    if (dev != TOPK_OK) return dev;
+    if (launch_page_transform(raw_indices, batch, k, page_table, page_table_stride, log2_exact(page_size),
+                              out_indices, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TOPK_ECUDA;
+    return TOPK_OK;
+}
+
+topk_status_t topk_key_map(const float* x, int64_t n, uint32_t* keys, topk_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !keys))) return TOPK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(keys) % 4) return TOPK_EALIGN;
+    const topk_status_t dev = check_device();
+    if (dev != TOPK_OK) return dev;
+    if (launch_key_map(x, n, keys, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TOPK_ECUDA;
+    return TOPK_OK;
+}
+
+topk_status_t topk_read_flags(void* workspace, uint32_t* flags_host, int32_t clear, topk_stream_t stream) {
+    if (!workspace || !flags_host) return TOPK_EINVAL;
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return TOPK_EALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    auto* hdr = static_cast<PlanHeader*>(workspace);
+    if (cudaMemcpyAsync(flags_host, &hdr->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return TOPK_ECUDA;
+    if (clear && cudaMemsetAsync(&hdr->flags, 0, sizeof(uint32_t), st) != cudaSuccess) return TOPK_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TOPK_ECUDA;
+    return TOPK_OK;
+}
+
+}  // extern "C"

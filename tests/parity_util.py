@@ -1,0 +1,75 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and compare it with the CPU oracle row by row (as sorted index sets)."""
+from __future__ import annotations
+
+import contextlib
+import os
+
+import numpy as np
+
+import oracle
+
+NTHREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def to_device(wl):
+    import torch
+
+    dev = torch.device("cuda", 0)
+    return (torch.from_numpy(wl.scores).to(dev), torch.from_numpy(wl.seq_lens).to(dev),
+            torch.from_numpy(wl.page_table).to(dev))
+
+
+def run_gpu(wl, want_raw=True):
+    """Plan + transform on cuda:0; returns host (out, raw, flags)."""
+    import torch
+
+    from sparse_attention_indexer_uint32_gb300 import _lib, api
+
+    scores, seq_lens, table = to_device(wl)
+    out, raw, ws = api.topk_transform(scores, seq_lens, table, wl.page_size, wl.k, max_seq_len=wl.max_seq_len,
+                                      want_raw=want_raw)
+    torch.cuda.synchronize()
+    flags = _lib.topk_read_flags(ws)
+    return out.cpu().numpy(), (raw.cpu().numpy() if raw is not None else None), flags
+
+
+def compare(wl, out, raw, rows=None, check_raw=True):
+    """Asserts that the GPU rows equal the oracle's as sorted sets, that the
+    padding is -1, and that out is the page transform of raw slot by slot."""
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    o_out, o_raw, _ = oracle.topk_transform(wl.scores[rows], wl.seq_lens[rows], wl.page_table[rows], wl.page_size,
+                                            wl.k, max_seq_len=wl.max_seq_len, want_raw=True, nthreads=NTHREADS)
+    eff = np.clip(wl.seq_lens[rows].astype(np.int64), 0, wl.max_seq_len)
+    n = np.minimum(eff, wl.k)
+    slot = np.arange(wl.k)[None, :]
+    valid = slot < n[:, None]
+    g_out = out[rows]
+    assert (g_out[~valid] == -1).all(), "out padding is not -1"
+    big = np.iinfo(np.int64).max
+    srt = lambda a: np.sort(np.where(valid, a.astype(np.int64), big), axis=1)  # noqa: E731
+    bad = np.nonzero((srt(g_out) != srt(o_out)).any(axis=1))[0]
+    if check_raw and raw is not None:
+        g_raw = raw[rows]
+        assert (g_raw[~valid] == -1).all(), "raw padding is not -1"
+        bad_raw = np.nonzero((srt(g_raw) != srt(o_raw)).any(axis=1))[0]
+        assert len(bad_raw) == 0, f"raw set differs from the oracle in rows {rows[bad_raw][:10].tolist()}"
+        again = oracle.page_transform(g_raw, wl.page_table[rows], wl.page_size)
+        assert (again == g_out).all(), "out is not the page transform of raw slot by slot"
+    assert len(bad) == 0, f"out set differs from the oracle in rows {rows[bad][:10].tolist()}"
+
+
+@contextlib.contextmanager
+def tuning(**overrides):
+    """Temporarily overrides dispatch knobs of the CUDA library."""
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    old = _lib.topk_get_tuning()
+    new = _lib.topk_tuning_t(**old.as_dict())
+    for k, v in overrides.items():
+        setattr(new, k, v)
+    _lib.topk_set_tuning(new)
+    try:
+        yield
+    finally:
+        _lib.topk_set_tuning(old)

@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bit-exact comparison of the selected index sets (raw and transformed), the -1
+padding and slot alignment, on seeded inputs: the five benchmark workloads at
+their full sizes (all rows where the oracle is quick, otherwise sampled rows)
+and small ragged cases that span several tiles, every dispatch path and the
+degenerate inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from sparse_attention_indexer_uint32_gb300 import workloads
+from tests.parity_util import compare, run_gpu, tuning
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample_rows(batch, count, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(batch, size=min(count, batch), replace=False).tolist())
+    rows.update({0, batch - 1})
+    return np.array(sorted(rows))
+
+
+# ----------------------------------------------------------- the five workloads
+def test_tiny_workload():
+    wl = workloads.tiny()
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
+def test_decode_workload_sampled_rows():
+    wl = workloads.decode()
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw, rows=_sample_rows(wl.batch, 96))
+    assert flags == 0
+
+
+def test_throughput_workload_sampled_rows():
+    wl = workloads.throughput()
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw, rows=_sample_rows(wl.batch, 24))
+    assert flags == 0
+
+
+@pytest.mark.parametrize("batch", [1, 8, 32])
+def test_long_context_workload(batch):
+    wl = workloads.long_context(batch)
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw, rows=None if batch <= 8 else _sample_rows(batch, 8))
+    assert flags == 0
+
+
+def test_ragged_workload_all_rows():
+    wl = workloads.ragged()
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
+# ------------------------------------------------------------ small ragged cases
+DISTS = ["normal", "bf16", "int", "flat", "neginf"]
+
+
+@pytest.mark.parametrize("dist", DISTS)
+@pytest.mark.parametrize("k", [1, 37, 512, 2048])
+def test_random_ragged_single_block(dist, k):
+    wl = workloads.random_case(seed=DISTS.index(dist) * 10000 + k, batch=40, min_len=0, max_len=20011, k=k,
+                               page_size=64, dist=dist)
+    out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+@pytest.mark.parametrize("cluster", [2, 4, 8, 16])
+@pytest.mark.parametrize("dist", ["normal", "bf16", "flat", "neginf"])
+def test_cluster_path_forced(cluster, dist):
+    wl = workloads.random_case(seed=100 + cluster, batch=12, min_len=1, max_len=70001, k=700, page_size=16,
+                               dist=dist)
+    with tuning(long_threshold=0, long_threshold_small_batch=0, cluster_size=cluster):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+@pytest.mark.parametrize("cluster", [1, 8])
+@pytest.mark.parametrize("dist", ["normal", "int", "flat"])
+def test_two_pass_streaming_forced(cluster, dist):
+    wl = workloads.random_case(seed=200 + cluster, batch=10, min_len=3000, max_len=90000, k=300, page_size=32,
+                               dist=dist)
+    thr = 0 if cluster > 1 else 1 << 30
+    with tuning(force_two_pass=1, long_threshold=thr, long_threshold_small_batch=thr):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+@pytest.mark.parametrize("cluster", [1, 8])
+@pytest.mark.parametrize("dist", ["normal", "bf16"])
+def test_ungated_first_pass(cluster, dist):
+    wl = workloads.random_case(seed=300 + cluster, batch=9, min_len=1000, max_len=60000, k=1024, page_size=8,
+                               dist=dist)
+    thr = 0 if cluster > 1 else 1 << 30
+    with tuning(disable_gate=1, long_threshold=thr, long_threshold_small_batch=thr):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+@pytest.mark.parametrize("samples", [32, 64])
+def test_few_samples_gate_misses(samples):
+    """With very few samples the gate is often too tight or too loose; the
+    fallbacks must still give the exact answer."""
+    wl = workloads.random_case(seed=400 + samples, batch=16, min_len=5000, max_len=40000, k=2048, page_size=64,
+                               dist="normal")
+    with tuning(samples=samples):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+def test_trend_rows_cluster():
+    """Rows with a positional trend (the gate's sample must not alias)."""
+    wl = workloads.long_context(batch=2, seq_len=300000)
+    with tuning(long_threshold=0, long_threshold_small_batch=0):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+# ------------------------------------------------------------------ edge cases
+def _make(scores, lens, k, page_size=1, max_seq_len=None, table=None):
+    scores = np.ascontiguousarray(scores, np.float32)
+    B, S = scores.shape
+    max_seq_len = S if max_seq_len is None else max_seq_len
+    pages = workloads.pages_for(S, page_size)
+    if table is None:
+        table = workloads.identity_table(B, pages)
+    return workloads.Workload("edge", scores, np.asarray(lens, np.int32), table, page_size, k, max_seq_len, True)
+
+
+def test_empty_and_tiny_rows():
+    rng = np.random.default_rng(1)
+    S = 64
+    scores = rng.standard_normal((8, S)).astype(np.float32)
+    wl = _make(scores, [0, 1, 2, 3, 4, 5, 63, 64], k=4)
+    out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+@pytest.mark.parametrize("k", [1, 2, 511, 512, 513, 2047, 2048])
+def test_k_boundaries(k):
+    rng = np.random.default_rng(k)
+    S = 4100
+    lens = [k - 1, k, k + 1, 4097, 4100, 2 * k + 3]
+    scores = rng.standard_normal((len(lens), S)).astype(np.float32)
+    wl = _make(scores, np.minimum(lens, S), k=k, page_size=4)
+    out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+def test_seq_len_flags():
+    from sparse_attention_indexer_uint32_gb300 import _lib  # noqa: F401
+
+    rng = np.random.default_rng(2)
+    S = 4096
+    scores = rng.standard_normal((4, S)).astype(np.float32)
+    wl = _make(scores, [-7, 5000, 3000, 100], k=64, max_seq_len=4000)
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags & 0x1 and flags & 0x2
+
+
+def test_special_values():
+    S = 9000
+    rng = np.random.default_rng(3)
+    base = rng.standard_normal(S).astype(np.float32)
+    rows = []
+    r = base.copy()
+    r[::3] = np.inf
+    rows.append(r)
+    r = base.copy()
+    r[::5] = -np.inf
+    r[1::5] = -0.0
+    r[2::5] = 0.0
+    rows.append(r)
+    r = np.where(np.arange(S) % 2 == 0, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+    rows.append(r)
+    r = np.full(S, -np.inf, np.float32)
+    rows.append(r)
+    r = base.copy()
+    r[::7] = np.float32(np.nan)
+    r.view(np.uint32)[3::11] = 0xFFC00001  # negative NaNs
+    r.view(np.uint32)[4::13] = 0x7F800001  # positive NaN with another payload
+    rows.append(r)
+    r = np.float32(1e-45) * (np.arange(S) % 17).astype(np.float32)  # denormals
+    rows.append(r)
+    scores = np.stack(rows)
+    wl = _make(scores, [S] * len(rows), k=1000, page_size=2)
+    out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+def test_row_stride_larger_than_length_and_unaligned_tail():
+    rng = np.random.default_rng(4)
+    S = 12004
+    lens = [12001, 11999, 7, 5003, 12004, 4097]
+    scores = rng.standard_normal((len(lens), S)).astype(np.float32)
+    for b, L in enumerate(lens):
+        scores[b, L:] = np.inf  # would win if a read past seq_len leaked in
+    wl = _make(scores, lens, k=512, page_size=64)
+    out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+@pytest.mark.parametrize("page_size", [1, 2, 128, 1 << 16])
+def test_page_sizes_permuted(page_size):
+    wl = workloads.random_case(seed=500 + page_size, batch=6, min_len=100, max_len=30000, k=256,
+                               page_size=page_size, dist="normal", permuted=True)
+    out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
+def test_repeat_runs_identical_sets():
+    wl = workloads.random_case(seed=9, batch=24, min_len=0, max_len=80000, k=512, page_size=64, dist="bf16")
+    ref_out, ref_raw, _ = run_gpu(wl)
+    for _ in range(10):
+        out, raw, _ = run_gpu(wl)
+        assert (np.sort(out, axis=1) == np.sort(ref_out, axis=1)).all()
+        assert (np.sort(raw, axis=1) == np.sort(ref_raw, axis=1)).all()
+    compare(wl, ref_out, ref_raw)

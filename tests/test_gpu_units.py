@@ -1,0 +1,156 @@
+"""GPU checks of the single steps exposed at the C ABI: the key map, the
+stand-alone page transform and the plan, plus argument errors."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_attention_indexer_uint32_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    return _lib
+
+
+def test_key_map_orders_every_float():
+    """Walk every non-NaN fp32 in increasing IEEE order: the keys must increase
+    strictly, except that -0.0 and +0.0 share a key; NaNs sit outside."""
+    import torch
+
+    lib = _lib()
+    dev = torch.device("cuda", 0)
+    chunk = 1 << 26
+    # increasing order: -inf (0xFF800000) down the bit patterns to -0.0
+    # (0x80000000), then +0.0 (0x00000000) up to +inf (0x7F800000)
+    segments = [(0xFF800000, 0x80000000, -1), (0x00000000, 0x7F800000, +1)]
+    last_key = None
+    for seg, (start, stop, step) in enumerate(segments):
+        count = abs(stop - start) + 1
+        for off in range(0, count, chunk):
+            n = min(chunk, count - off)
+            bits = start + step * (off + torch.arange(n, device=dev, dtype=torch.int64))
+            b32 = torch.where(bits >= 2 ** 31, bits - 2 ** 32, bits).to(torch.int32)
+            keys = torch.empty(n, dtype=torch.int32, device=dev)
+            lib.topk_key_map(b32.view(torch.float32), n, keys)
+            k64 = keys.to(torch.int64).bitwise_and(0xFFFFFFFF)
+            assert bool((k64[1:] > k64[:-1]).all()), f"keys not increasing near bits {start + step * off:#x}"
+            first = int(k64[0])
+            if last_key is not None:
+                if seg == 1 and off == 0:
+                    assert first == last_key, "-0.0 and +0.0 must share a key"
+                else:
+                    assert first > last_key
+            last_key = int(k64[-1])
+    nan_bits = np.array([0x7FC00000, 0x7F800001, 0xFFC00000, 0xFF800001], dtype=np.uint32)
+    x = torch.from_numpy(nan_bits.view(np.float32)).to(dev)
+    inf = torch.tensor([np.inf, -np.inf], dtype=torch.float32, device=dev)
+    k_nan = torch.empty(4, dtype=torch.int32, device=dev)
+    k_inf = torch.empty(2, dtype=torch.int32, device=dev)
+    lib.topk_key_map(x, 4, k_nan)
+    lib.topk_key_map(inf, 2, k_inf)
+    kn = k_nan.cpu().numpy().view(np.uint32).astype(np.int64)
+    ki = k_inf.cpu().numpy().view(np.uint32).astype(np.int64)
+    assert kn[0] > ki[0] and kn[1] > ki[0] and kn[0] > kn[1]  # +NaN above +inf, larger payload higher
+    assert kn[2] < ki[1] and kn[3] < ki[1] and kn[2] < kn[3]  # -NaN below -inf, larger payload lower
+
+
+def test_page_transform_standalone_matches_oracle():
+    import torch
+
+    lib = _lib()
+    rng = np.random.default_rng(0)
+    for P in (1, 64, 128):
+        B, k, NP = 33, 517, 300
+        table = rng.permutation(B * NP).astype(np.int32).reshape(B, NP)
+        raw = rng.integers(-1, NP * P, size=(B, k)).astype(np.int32)
+        raw[:, -5:] = -1
+        expect = oracle.page_transform(raw, table, P)
+        dev = torch.device("cuda", 0)
+        raw_d = torch.from_numpy(raw).to(dev)
+        table_d = torch.from_numpy(table).to(dev)
+        out = torch.empty_like(raw_d)
+        lib.topk_page_transform(raw_d, B, k, table_d, NP, P, out)
+        assert (out.cpu().numpy() == expect).all()
+
+
+def test_plan_lists_match_oracle_classification():
+    import torch
+
+    lib = _lib()
+    rng = np.random.default_rng(1)
+    for batch, max_len in ((5, 1 << 20), (200, 300000), (8192, 8192)):
+        lens = rng.integers(-5, max_len + 1000, size=batch).astype(np.int32)
+        dev = torch.device("cuda", 0)
+        seq = torch.from_numpy(lens).to(dev)
+        nbytes = lib.topk_plan_workspace_bytes(batch)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        lib.topk_plan(seq, batch, max_len, ws)
+        torch.cuda.synchronize()
+        host = ws.cpu().numpy()
+        hdr = host[:64].view(np.int32)
+        t = lib.topk_get_tuning()
+        thr = t.long_threshold_small_batch if batch <= t.small_batch_max else t.long_threshold
+        eff, is_long, flags = oracle.plan_classify(lens, max_len, thr)
+        n_long, n_short = int(hdr[4]), int(hdr[5])
+        lists = host[64:64 + 8 * batch].view(np.int32)
+        long_rows, short_rows = lists[:n_long], lists[batch:batch + n_short]
+        assert sorted(long_rows.tolist()) == np.nonzero(is_long)[0].tolist()
+        assert sorted(short_rows.tolist()) == np.nonzero(~is_long)[0].tolist()
+        assert int(hdr[6]) == flags
+        # longest first (by half-octave bucket)
+        for rows in (long_rows, short_rows):
+            L = eff[rows].astype(np.int64)
+            bl = np.where(L > 0, np.floor(np.log2(np.maximum(L, 1))).astype(np.int64) + 1, 0)
+            bucket = np.where(bl >= 2, 2 * bl + ((L >> np.maximum(bl - 2, 0)) & 1), 2 * bl)
+            assert (np.diff(bucket) <= 0).all()
+
+
+def test_argument_errors_raise():
+    import torch
+
+    lib = _lib()
+    dev = torch.device("cuda", 0)
+    scores = torch.zeros((2, 64), dtype=torch.float32, device=dev)
+    seq = torch.full((2,), 64, dtype=torch.int32, device=dev)
+    table = torch.zeros((2, 1), dtype=torch.int32, device=dev)
+    out = torch.empty((2, 8), dtype=torch.int32, device=dev)
+    ws = torch.zeros(lib.topk_plan_workspace_bytes(2), dtype=torch.uint8, device=dev)
+    lib.topk_plan(seq, 2, 64, ws)
+    cases = [
+        dict(k=0), dict(k=2049), dict(page_size=3), dict(row_stride=62), dict(page_table_stride=0),
+        dict(max_seq_len=128),
+    ]
+    for over in cases:
+        args = dict(scores=scores, row_stride=64, seq_lens=seq, batch=2, max_seq_len=64, page_table=table,
+                    page_table_stride=1, page_size=64, k=8, out_indices=out, out_raw_indices_or_null=None,
+                    workspace=ws)
+        args.update(over)
+        with pytest.raises(lib.TopkError) as e:
+            lib.topk_transform(**args)
+        assert e.value.status in (lib.TOPK_EINVAL, lib.TOPK_EALIGN)
+    with pytest.raises(lib.TopkError):
+        lib.topk_transform(scores.view(-1)[1:], 64, seq, 2, 60, table, 1, 64, 8, out, None, ws)  # misaligned
+
+
+def test_plan_mismatch_is_flagged_and_nothing_written():
+    import torch
+
+    lib = _lib()
+    dev = torch.device("cuda", 0)
+    wl = workloads.random_case(seed=1, batch=4, min_len=100, max_len=1000, k=16, page_size=4)
+    scores = torch.from_numpy(wl.scores).to(dev)
+    seq = torch.from_numpy(wl.seq_lens).to(dev)
+    table = torch.from_numpy(wl.page_table).to(dev)
+    ws = torch.zeros(lib.topk_plan_workspace_bytes(4), dtype=torch.uint8, device=dev)
+    lib.topk_plan(seq, 4, wl.max_seq_len - 4, ws)  # planned for another max_seq_len
+    out = torch.full((4, 16), -7, dtype=torch.int32, device=dev)
+    lib.topk_transform(scores, wl.row_stride, seq, 4, wl.max_seq_len, table, wl.page_table.shape[1], 4, 16, out,
+                       None, ws)
+    torch.cuda.synchronize()
+    assert lib.topk_read_flags(ws) & lib.TOPK_FLAG_PLAN_MISMATCH
+    assert (out.cpu().numpy() == -7).all()
