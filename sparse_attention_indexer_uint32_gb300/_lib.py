@@ -99,8 +99,17 @@ def library() -> ctypes.CDLL:
 
 
 def _check(fn: str, status: int) -> None:
-    if status != TOPK_OK:
-        raise TopkError(fn, status)
+    if status == TOPK_OK:
+        return
+    err = TopkError(fn, status)
+    if status == TOPK_ECUDA:
+        # Surface the CUDA runtime's own message (for example a fault left by
+        # an earlier asynchronous launch) next to the library status.
+        try:
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001
+            raise err from e
+    raise err
 
 
 def _stream(stream, device) -> int:

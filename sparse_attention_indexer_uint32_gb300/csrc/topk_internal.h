@@ -83,7 +83,8 @@ struct __align__(16) Control {
     uint32_t rank_cnt[kMaxCluster];  // per-rank emitted counts (output placement)
     uint32_t rank_eq[kMaxCluster];   // per-rank copies of the threshold key (tie quotas)
     uint32_t err;
-    uint32_t pad[3];
+    uint32_t res_local;   // the local (un-merged) count of the bin found by the last scan
+    uint32_t pad[2];
 };
 
 struct Layout {

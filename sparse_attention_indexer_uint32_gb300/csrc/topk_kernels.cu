@@ -92,6 +92,7 @@ __device__ __forceinline__ int32_t page_map(const int32_t* pt_row, int32_t log2_
 
 struct ScanResult {
     uint32_t bin, above, count, total;
+    uint32_t local;  // this block's own count in `bin` (differs from `count` only in a cluster)
 };
 
 struct Smem {
@@ -123,7 +124,8 @@ __device__ __forceinline__ void clear_hist(uint32_t* h, int tid) {
 // total is below `need`, bin is 0xffffffff.  Every thread of the block must
 // call it; it contains two block barriers and reads `h` before the first.
 template <int NT>
-__device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need, int tid) {
+__device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need, int tid,
+                                const uint32_t* h_local = nullptr) {
     constexpr int BPT = kBins / NT;
     static_assert(BPT == 4 || BPT == 8, "bins per thread");
     const int lane = tid & 31, warp = tid >> 5;
@@ -160,6 +162,7 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
                 s.ctl->res_bin = static_cast<uint32_t>(base + i);
                 s.ctl->res_above = acc;
                 s.ctl->res_count = v[i];
+                s.ctl->res_local = h_local ? h_local[base + i] : v[i];
                 break;
             }
             acc += v[i];
@@ -170,6 +173,7 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
     r.bin = s.ctl->res_bin;
     r.above = s.ctl->res_above;
     r.count = s.ctl->res_count;
+    r.local = s.ctl->res_local;
     r.total = total;
     return r;
 }
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                 hm = s.hist_m;
             }
             const bool overflow = (C > 1) ? (hm[kSlotOverflow] != 0u) : (local_ovf != 0u);
-            ScanResult sr = scan_find<NT>(s, hm, Kp, tid);
+            ScanResult sr = scan_find<NT>(s, hm, Kp, tid, s.hist_a);
 
             // ----------------------------------------------------- 3. resolve
             uint32_t r_lo, r_hi, G, cnt, local_cnt = 0;
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                            : static_cast<uint32_t>(min_u64(0xffffffffull, lo + ((b + 1) << shift) - 1));
                 cnt = sr.count;
                 stream_mode = overflow;
-                local_cnt = s.hist_a[sr.bin];
+                local_cnt = sr.local;
             }
             clear_hist<NT>(s.hist_a, tid);
             uint32_t* h_next = s.hist_b;
@@ -655,13 +659,13 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                     cluster_merge<NT, C>(s, h_next, rank, tid);
                     hr = s.hist_m;
                 }
-                sr = scan_find<NT>(s, hr, Kp - G, tid);
+                sr = scan_find<NT>(s, hr, Kp - G, tid, h_next);
                 if (sr.bin >= static_cast<uint32_t>(kBins)) {  // cannot happen: the bin holds >= need
                     atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
                     clear_hist<NT>(h_next, tid);
                     break;
                 }
-                local_cnt = h_next[sr.bin];
+                local_cnt = sr.local;
                 G += sr.above;
                 const uint64_t b = sr.bin;
                 const uint32_t nlo = static_cast<uint32_t>(r_lo + (b << sh));
