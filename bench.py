@@ -43,6 +43,10 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 
 
+def log(*a):
+    print(f"[bench {time.strftime('%H:%M:%S')}]", *a, file=sys.stderr, flush=True)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -293,9 +297,11 @@ def oracle_sample_time(wl, target_s: float = 12.0):
 
 
 def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: int, full: bool):
+    log("workload", name)
     wl = build_workload(name)
     nbytes = wl.algorithmic_bytes()
     r = time_gpu(wl, steps, warmup, local, world, want_clocks=full)
+    log("timed", name, f"{r['total_ms'] / steps:.4f} ms/step", "flags", r["flags"])
     peak, peak_kind = measured_peak()
     ms_step = r["total_ms"] / steps
     sel_avg = statistics.mean(r["select_ms"])
@@ -320,11 +326,13 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
     if full:
         e2e_steps = max(3, min(steps, 10))
         ms, h2d, d2h = time_e2e(wl, e2e_steps, 2, local)
+        log("e2e", f"{ms:.3f} ms/step")
         line["e2e"] = {"value": round(nbytes / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
         line["clocks"] = r["clocks"]
         if rank == 0 and world == 1:
             line["cpu_baseline"] = oracle_sample_time(wl)
+            log("cpu baseline", line["cpu_baseline"])
     return line
 
 

@@ -164,6 +164,15 @@ topk_status_t topk_read_flags(void* workspace, uint32_t* flags_host, int32_t cle
 const char* topk_status_string(topk_status_t status);
 
 /*
+ * Text of the last CUDA failure that made a call on this host thread return
+ * TOPK_ECUDA ("" if none): the failing step and the runtime's error name and
+ * message.  The library resets the CUDA runtime's per-thread error state
+ * after such a failure, so it does not resurface in the caller's own
+ * cudaGetLastError().  The pointer stays valid for the thread's lifetime.
+ */
+const char* topk_last_error_string(void);
+
+/*
  * Dispatch knobs.  Defaults are the GB300 settings; tests use the overrides
  * to drive every path.  The values are process-wide and take effect for
  * calls made after topk_set_tuning returns; do not change them while another

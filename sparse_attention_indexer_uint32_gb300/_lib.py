@@ -36,6 +36,7 @@ EXPORTED = (
     "topk_key_map",
     "topk_read_flags",
     "topk_status_string",
+    "topk_last_error_string",
     "topk_get_tuning",
     "topk_set_tuning",
 )
@@ -43,7 +44,8 @@ EXPORTED = (
 
 class TopkError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} failed: {status} ({topk_status_string(status)})")
+        detail = f"; {topk_last_error_string()}" if status == TOPK_ECUDA else ""
+        super().__init__(f"{fn} failed: {status} ({topk_status_string(status)}){detail}")
         self.status = status
 
 
@@ -84,6 +86,8 @@ def _load() -> ctypes.CDLL:
     lib.topk_read_flags.restype = ctypes.c_int
     lib.topk_status_string.argtypes = [ctypes.c_int]
     lib.topk_status_string.restype = ctypes.c_char_p
+    lib.topk_last_error_string.argtypes = []
+    lib.topk_last_error_string.restype = ctypes.c_char_p
     lib.topk_get_tuning.argtypes = [ctypes.POINTER(topk_tuning_t)]
     lib.topk_get_tuning.restype = ctypes.c_int
     lib.topk_set_tuning.argtypes = [ctypes.POINTER(topk_tuning_t)]
@@ -124,6 +128,10 @@ def _ptr(t: torch.Tensor | None) -> int | None:
 
 def topk_status_string(status: int) -> str:
     return _lib.topk_status_string(status).decode()
+
+
+def topk_last_error_string() -> str:
+    return _lib.topk_last_error_string().decode()
 
 
 def topk_plan_workspace_bytes(batch: int) -> int:

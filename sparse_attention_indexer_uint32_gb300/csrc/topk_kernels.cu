@@ -20,6 +20,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -982,19 +983,34 @@ __global__ void key_map_kernel(const float* x, int64_t n, uint32_t* keys) {
         keys[i] = score_key(x[i]);
 }
 
+// Raises the kernel's dynamic shared-memory limit to the device's opt-in
+// maximum (and allows 16-block clusters) once per device.  The limit is only
+// a ceiling, so every launch below it stays valid whatever its size.
+template <int NT, int C>
+cudaError_t ensure_attributes() {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(select_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return e;
+    if (C > 8) {
+        e = cudaFuncSetAttribute(select_kernel<NT, C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    done.fetch_or(bit, std::memory_order_release);
+    return cudaSuccess;
+}
+
 template <int NT, int C>
 cudaError_t launch_select_t(const SelectParams& p, int grid_units, size_t smem, cudaStream_t stream) {
-    auto kern = select_kernel<NT, C>;
-    static size_t smem_set = 0;
-    if (smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        if (C > 8) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-        }
-        smem_set = smem;
-    }
+    cudaError_t e = ensure_attributes<NT, C>();
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_units * C));
     cfg.blockDim = dim3(NT);
@@ -1009,13 +1025,13 @@ cudaError_t launch_select_t(const SelectParams& p, int grid_units, size_t smem, 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return cudaLaunchKernelEx(&cfg, select_kernel<NT, C>, p);
 }
 
 template <int NT, int C>
 cudaError_t occupancy_t(size_t smem, int* units) {
     auto kern = select_kernel<NT, C>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = ensure_attributes<NT, C>();
     if (e != cudaSuccess) return e;
     if (C == 1) {
         int per_sm = 0, dev = 0, sms = 0;
@@ -1025,10 +1041,6 @@ cudaError_t occupancy_t(size_t smem, int* units) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         *units = per_sm * sms;
         return cudaSuccess;
-    }
-    if (C > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C * 64);
@@ -1046,6 +1058,15 @@ cudaError_t occupancy_t(size_t smem, int* units) {
     if (e != cudaSuccess) return e;
     *units = clusters;
     return cudaSuccess;
+}
+
+template <typename... Args>
+cudaError_t launch_plain(void (*kern)(Args...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace
@@ -1076,23 +1097,22 @@ cudaError_t select_occupancy(int cluster, size_t smem, int* units_out) {
 
 cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
                         void* workspace, cudaStream_t stream) {
-    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, batch, max_seq_len, long_threshold, workspace);
-    return cudaGetLastError();
+    return launch_plain(plan_kernel, dim3(1), dim3(1024), stream, seq_lens, batch, max_seq_len, long_threshold,
+                        workspace);
 }
 
 cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
                                   int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream) {
     const int64_t n = static_cast<int64_t>(batch) * k;
     const int blocks = static_cast<int>(min_i64((n + 255) / 256, 152 * 8));
-    page_transform_kernel<<<blocks, 256, 0, stream>>>(raw, batch, k, page_table, pt_stride, log2_page, out);
-    return cudaGetLastError();
+    return launch_plain(page_transform_kernel, dim3(blocks), dim3(256), stream, raw, batch, k, page_table, pt_stride,
+                        log2_page, out);
 }
 
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
     const int blocks = static_cast<int>(min_i64((n + 255) / 256, 152 * 16));
-    key_map_kernel<<<blocks, 256, 0, stream>>>(x, n, keys);
-    return cudaGetLastError();
+    return launch_plain(key_map_kernel, dim3(blocks), dim3(256), stream, x, n, keys);
 }
 
 }  // namespace topkidx

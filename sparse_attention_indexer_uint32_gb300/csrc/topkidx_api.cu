@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -18,6 +19,16 @@ using namespace topkidx;
 namespace {
 
 std::mutex g_mutex;
+thread_local char g_last_error[256] = "";
+
+// Records a failed CUDA call for topk_last_error_string() and resets the
+// runtime's per-thread error state, so a rejected launch does not surface
+// later in an unrelated caller's cudaGetLastError().
+topk_status_t cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+    (void)cudaGetLastError();
+    return TOPK_ECUDA;
+}
 
 // Thresholds after SGLang PR #26788 (commit "Fuse the cluster/non-cluster
 // split for small batch": long rows above 32K for small batches, 64K
@@ -36,15 +47,16 @@ int log2_exact(int64_t x) {
 
 topk_status_t check_device() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ECUDA;
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess) return cuda_fail(ge, "cudaGetDevice");
     static std::map<int, topk_status_t> known;
     std::lock_guard<std::mutex> lock(g_mutex);
     auto it = known.find(dev);
     if (it != known.end()) return it->second;
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return TOPK_ECUDA;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     const topk_status_t st = (major == 10 && minor == 3) ? TOPK_OK : TOPK_EDEVICE;
     known[dev] = st;
     return st;
@@ -105,7 +117,13 @@ topk_status_t resident_units(int cluster, size_t smem, int* units) {
         }
     }
     int u = 0;
-    if (select_occupancy(cluster, smem, &u) != cudaSuccess || u <= 0) return TOPK_ECUDA;
+    const cudaError_t e = select_occupancy(cluster, smem, &u);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (u <= 0) {
+        snprintf(g_last_error, sizeof(g_last_error), "select kernel (cluster %d, %zu B smem) cannot be resident",
+                 cluster, smem);
+        return TOPK_ECUDA;
+    }
     std::lock_guard<std::mutex> lock(g_mutex);
     cache[key] = u;
     *units = u;
@@ -117,6 +135,8 @@ topk_status_t resident_units(int cluster, size_t smem, int* units) {
 extern "C" {
 
 size_t topk_plan_workspace_bytes(int32_t batch) { return plan_bytes(batch); }
+
+const char* topk_last_error_string(void) { return g_last_error; }
 
 const char* topk_status_string(topk_status_t status) {
     switch (status) {
@@ -161,9 +181,9 @@ topk_status_t topk_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_
     if (dev != TOPK_OK) return dev;
     topk_tuning_t t;
     topk_get_tuning(&t);
-    if (launch_plan(seq_lens, batch, max_seq_len, long_threshold(t, batch), workspace,
-                    reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return TOPK_ECUDA;
+    const cudaError_t e = launch_plan(seq_lens, batch, max_seq_len, long_threshold(t, batch), workspace,
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "plan launch");
     return TOPK_OK;
 }
 
@@ -223,7 +243,8 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         q.cap = c.cap;
         q.samples = c.samples;
         const int grid = batch < units ? batch : units;
-        if (launch_select(q, c.cluster, grid, c.smem, st) != cudaSuccess) return TOPK_ECUDA;
+        const cudaError_t e = launch_select(q, c.cluster, grid, c.smem, st);
+        if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
     }
     {
         const PathConfig c = path_config(1, k, t);
@@ -245,7 +266,8 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         // same number of rows when all rows are short.
         const int per_unit = (batch + units - 1) / units;
         const int grid = (batch + per_unit - 1) / per_unit;
-        if (launch_select(q, 1, grid, c.smem, st) != cudaSuccess) return TOPK_ECUDA;
+        const cudaError_t e = launch_select(q, 1, grid, c.smem, st);
+        if (e != cudaSuccess) return cuda_fail(e, "select launch");
     }
     return TOPK_OK;
 }
@@ -261,9 +283,10 @@ topk_status_t topk_page_transform(const int32_t* raw_indices, int32_t batch, int
         return TOPK_EALIGN;
     const topk_status_t dev = check_device();
     if (dev != TOPK_OK) return dev;
-    if (launch_page_transform(raw_indices, batch, k, page_table, page_table_stride, log2_exact(page_size),
-                              out_indices, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return TOPK_ECUDA;
+    const cudaError_t e = launch_page_transform(raw_indices, batch, k, page_table, page_table_stride,
+                                                log2_exact(page_size), out_indices,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "page transform launch");
     return TOPK_OK;
 }
 
@@ -272,7 +295,8 @@ topk_status_t topk_key_map(const float* x, int64_t n, uint32_t* keys, topk_strea
     if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(keys) % 4) return TOPK_EALIGN;
     const topk_status_t dev = check_device();
     if (dev != TOPK_OK) return dev;
-    if (launch_key_map(x, n, keys, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return TOPK_ECUDA;
+    const cudaError_t e = launch_key_map(x, n, keys, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "key map launch");
     return TOPK_OK;
 }
 
@@ -281,10 +305,11 @@ topk_status_t topk_read_flags(void* workspace, uint32_t* flags_host, int32_t cle
     if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return TOPK_EALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     auto* hdr = static_cast<PlanHeader*>(workspace);
-    if (cudaMemcpyAsync(flags_host, &hdr->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return TOPK_ECUDA;
-    if (clear && cudaMemsetAsync(&hdr->flags, 0, sizeof(uint32_t), st) != cudaSuccess) return TOPK_ECUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return TOPK_ECUDA;
+    cudaError_t e = cudaMemcpyAsync(flags_host, &hdr->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "flag copy");
+    if (clear && (e = cudaMemsetAsync(&hdr->flags, 0, sizeof(uint32_t), st)) != cudaSuccess)
+        return cuda_fail(e, "flag reset");
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
     return TOPK_OK;
 }
 

@@ -33,7 +33,7 @@ def test_header_declares_the_documented_entry_points():
     names = declared_functions()
     for required in ("topk_plan", "topk_transform", "topk_plan_workspace_bytes", "topk_page_transform",
                      "topk_key_map", "topk_read_flags", "topk_status_string", "topk_get_tuning",
-                     "topk_set_tuning"):
+                     "topk_set_tuning", "topk_last_error_string"):
         assert required in names
 
 
@@ -49,6 +49,7 @@ def test_status_strings(lib):
         assert isinstance(lib.topk_status_string(code), str) and lib.topk_status_string(code)
     assert lib.topk_status_string(0) == "ok"
     assert lib.topk_status_string(99) == "unknown status"
+    assert lib.topk_last_error_string() == ""  # no CUDA call has failed on this thread
 
 
 def test_workspace_bytes(lib):
