@@ -160,6 +160,38 @@ topk_status_t topk_key_map(const float* x, int64_t n, uint32_t* keys, topk_strea
  */
 topk_status_t topk_read_flags(void* workspace, uint32_t* flags_host, int32_t clear, topk_stream_t stream);
 
+/*
+ * Allocation-free variant of topk_plan + topk_transform (the pages have no
+ * counterpart; this is a convenience of this library).
+ *
+ * For callers that cannot allocate device memory -- for example a plugin or
+ * an allocator-managed runtime that only hands out its inputs and outputs and
+ * must not call cudaMalloc behind its allocator's back -- this call keeps the
+ * plan's work lists in a fixed device array owned by the library instead of
+ * a caller workspace.  Every GPU that loads the library holds that array
+ * (about 128 KiB) until the process exits.  Arguments and outputs are those
+ * of topk_transform; the caller still passes scores, seq_lens, the page table
+ * and the output buffers.
+ *
+ *   - batch must be <= TOPK_NOALLOC_MAX_BATCH; larger batches return
+ *     TOPK_ENOSPACE and enqueue nothing (use topk_plan + topk_transform with
+ *     a caller workspace instead).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its contents in
+ *     it.  Calls whose work can overlap on the GPU (two streams, or two host
+ *     threads, at once) race on it: serialise them.
+ *   - The array's flag word is not exposed; use topk_plan + topk_transform +
+ *     topk_read_flags when the clamp/timeout flags are needed.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define TOPK_NOALLOC_MAX_BATCH 16384
+topk_status_t topk_transform_noalloc(const float* scores, int64_t row_stride, const int32_t* seq_lens,
+                                     int32_t batch, int32_t max_seq_len, const int32_t* page_table,
+                                     int64_t page_table_stride, int32_t page_size, int32_t k,
+                                     int32_t* out_indices, int32_t* out_raw_indices_or_null, topk_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* topk_status_string(topk_status_t status);
 

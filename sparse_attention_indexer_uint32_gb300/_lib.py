@@ -28,10 +28,13 @@ TOPK_FLAG_PLAN_MISMATCH = 0x4
 TOPK_FLAG_TIMEOUT = 0x8
 TOPK_FLAG_INTERNAL = 0x10
 
+TOPK_NOALLOC_MAX_BATCH = 16384
+
 EXPORTED = (
     "topk_plan_workspace_bytes",
     "topk_plan",
     "topk_transform",
+    "topk_transform_noalloc",
     "topk_page_transform",
     "topk_key_map",
     "topk_read_flags",
@@ -78,6 +81,8 @@ def _load() -> ctypes.CDLL:
     lib.topk_plan.restype = ctypes.c_int
     lib.topk_transform.argtypes = [p, i64, p, i32, i32, p, i64, i32, i32, p, p, p, p]
     lib.topk_transform.restype = ctypes.c_int
+    lib.topk_transform_noalloc.argtypes = [p, i64, p, i32, i32, p, i64, i32, i32, p, p, p]
+    lib.topk_transform_noalloc.restype = ctypes.c_int
     lib.topk_page_transform.argtypes = [p, i32, i32, p, i64, i32, p, p]
     lib.topk_page_transform.restype = ctypes.c_int
     lib.topk_key_map.argtypes = [p, i64, p, p]
@@ -154,6 +159,16 @@ def topk_transform(scores: torch.Tensor, row_stride: int, seq_lens: torch.Tensor
         _ptr(scores), row_stride, _ptr(seq_lens), batch, max_seq_len, _ptr(page_table), page_table_stride,
         page_size, k, _ptr(out_indices), _ptr(out_raw_indices_or_null), _ptr(workspace),
         _stream(stream, scores.device)))
+
+
+def topk_transform_noalloc(scores: torch.Tensor, row_stride: int, seq_lens: torch.Tensor, batch: int,
+                           max_seq_len: int, page_table: torch.Tensor, page_table_stride: int, page_size: int,
+                           k: int, out_indices: torch.Tensor, out_raw_indices_or_null: torch.Tensor | None,
+                           stream=None) -> None:
+    """Plan + transform without a caller workspace (batch <= TOPK_NOALLOC_MAX_BATCH)."""
+    _check("topk_transform_noalloc", _lib.topk_transform_noalloc(
+        _ptr(scores), row_stride, _ptr(seq_lens), batch, max_seq_len, _ptr(page_table), page_table_stride,
+        page_size, k, _ptr(out_indices), _ptr(out_raw_indices_or_null), _stream(stream, scores.device)))
 
 
 def topk_page_transform(raw_indices: torch.Tensor, batch: int, k: int, page_table: torch.Tensor,
