@@ -220,8 +220,8 @@ typedef struct {
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */
     int32_t candidate_capacity;         /* 0: automatic; else candidates per block, 2048..16384,
                                            a multiple of 64                                      */
-    int32_t samples;                    /* 0: automatic; else gate samples per row, 32..4096,
-                                           a multiple of 32                                      */
+    int32_t samples;                    /* 0: automatic; else at most this many gate samples per
+                                           row, 32..2048, a multiple of 32                       */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -14,7 +14,7 @@ constexpr int kBinBits = 11;
 constexpr int kBinsX = kBins + 64;      // + control slots carried through cluster merges
 constexpr int kSlotOverflow = kBins;    // merged slot: some block's candidate buffer overflowed
 constexpr int kFinish = 32;             // a warp-wide compare-and-swap sort finishes <= 32 candidates
-constexpr int kSamplesPerThread = 4;    // gate samples held per thread
+constexpr int kMaxSamples = 2048;       // gate samples per row (held 2048 / threads per thread)
 constexpr int kItemsMax = 256;          // work items staged in shared memory per window
 constexpr int kMaxK = 2048;
 constexpr int kMaxCluster = 16;

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
     s.full = reinterpret_cast<uint64_t*>(smem_raw + lay.mbar);
     s.empty = s.full + p.stages;
 
+    constexpr int kSamplesPerThread = kMaxSamples / NT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = (C > 1) ? ptx::cluster_ctarank() : 0u;
     const uint32_t unit = (C > 1) ? ptx::cluster_id_x() : blockIdx.x;
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                             atomicOr(&s.ctl->err, TOPK_FLAG_TIMEOUT);
                             break;
                         }
-                    } else if (!ptx::mbar_try_wait(&s.empty[st], par)) {
+                    } else if (!ptx::mbar_test_wait(&s.empty[st], par)) {
                         break;
                     }
                 }
@@ -403,6 +404,11 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
             }
         };
 
+        // Samples per row: 1024 for rows up to 16K, more for longer rows.
+        auto samples_for = [&](uint32_t L) -> uint32_t {
+            const uint32_t m = L <= 16384u ? min(m_max, 1024u) : m_max;
+            return min(m, L);
+        };
         // Gate samples of the next non-trivial row are loaded one row ahead.
         float smp[kSamplesPerThread];
         auto load_samples = [&](int32_t j) {
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
             if (j >= nw) return;
             const int32_t L = s.it_len[j];
             if (L <= p.k) return;
-            const uint32_t M = min(m_max, static_cast<uint32_t>(L));
+            const uint32_t M = samples_for(static_cast<uint32_t>(L));
             const float* rowp = p.scores + static_cast<int64_t>(s.it_row[j]) * p.row_stride;
 #pragma unroll
             for (int q = 0; q < kSamplesPerThread; ++q) {
@@ -463,11 +469,19 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
             uint32_t lo = 0;
             int shift = 32 - kBinBits;
             {
-                const uint32_t M = min(m_max, static_cast<uint32_t>(L));
-                const uint64_t r64 =
-                    (2ull * M * Kp + static_cast<uint64_t>(L) - 1ull) / static_cast<uint64_t>(L) + 8ull;
-                if (!p.disable_gate && r64 < M) {
-                    const uint32_t r = static_cast<uint32_t>(r64);
+                // r = the sample rank used as the gate.  E samples are expected in the
+                // row's top k; r = E + 4 sqrt(E) + 4 keeps the chance that fewer than k
+                // elements pass the gate small (that case is detected and recounted),
+                // and r is raised to aim at half of the on-chip candidate capacity,
+                // since a tighter gate buys nothing once the candidates fit.
+                const uint32_t M = samples_for(static_cast<uint32_t>(L));
+                const float E = static_cast<float>(M) * static_cast<float>(Kp) / static_cast<float>(L);
+                const float r_safe = ceilf(E + 4.0f * sqrtf(E) + 4.0f);
+                const float r_fill = floorf(0.5f * static_cast<float>(cap) * C * static_cast<float>(M) /
+                                            static_cast<float>(L));
+                const float r_f = fmaxf(r_safe, r_fill);
+                if (!p.disable_gate && r_f < static_cast<float>(M)) {
+                    const uint32_t r = static_cast<uint32_t>(r_f);
                     uint32_t keys[kSamplesPerThread];
                     uint32_t kmax = 0;
 #pragma unroll
@@ -484,7 +498,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                     __syncthreads();
                     const ScanResult g = scan_find<NT>(s, s.hist_a, r, tid);
                     lo = g.bin << (32 - kBinBits);
-                    if (g.above + g.count > 2u * r && g.count > 1u) {
+                    if (g.above + g.count > r + r / 4u + 4u && g.count > 1u) {
                         // Refine inside the coarse bin on the next 11 bits.
 #pragma unroll
                         for (int q = 0; q < kSamplesPerThread; ++q) {
@@ -916,44 +930,79 @@ __device__ __forceinline__ int length_bucket(int32_t L) {
 // plan compacts the long items into a work list).  One block: every row is
 // classified long (clamped seq_len > threshold) or short, and each class is
 // written as a list ordered by half-octave length bucket, longest first, so
-// that the persistent kernels hand out the longest rows first.
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
-                                                    int32_t threshold, void* ws) {
-    __shared__ uint32_t cnt[2][64];
-    __shared__ uint32_t cur[2][64];
-    __shared__ uint32_t flags;
-    const int tid = threadIdx.x;
-    for (int i = tid; i < 128; i += blockDim.x) (&cnt[0][0])[i] = 0;
-    if (tid == 0) flags = 0;
-    __syncthreads();
-    for (int32_t b = tid; b < batch; b += blockDim.x) {
-        int32_t L = seq_lens[b];
-        if (L < 0) {
-            atomicOr(&flags, TOPK_FLAG_SEQ_NEGATIVE);
-            L = 0;
-        } else if (L > max_seq_len) {
-            atomicOr(&flags, TOPK_FLAG_SEQ_CLAMPED);
-            L = max_seq_len;
-        }
-        atomicAdd(&cnt[L > threshold ? 1 : 0][length_bucket(L)], 1u);
+// that the persistent kernels hand out the longest rows first.  Lengths are
+// loaded into registers up front (no dependent load chain), and the lanes of
+// a warp that share a (class, bucket) combine their atomics.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanPerThread = 16;
+
+__device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t max_seq_len, uint32_t* flags) {
+    if (L < 0) {
+        *flags |= TOPK_FLAG_SEQ_NEGATIVE;
+        return 0;
     }
-    __syncthreads();
-    if (tid < 2) {
-        uint32_t run = 0;
-        for (int k = 63; k >= 0; --k) {
-            cur[tid][k] = run;
-            run += cnt[tid][k];
-        }
-        cnt[tid][0] = run;  // total of the class (bucket 0 no longer needed)
+    if (L > max_seq_len) {
+        *flags |= TOPK_FLAG_SEQ_CLAMPED;
+        return max_seq_len;
     }
+    return L;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_lens, int32_t batch,
+                                                            int32_t max_seq_len, int32_t threshold, void* ws) {
+    __shared__ uint32_t cnt[128];
+    __shared__ uint32_t cur[128];
+    __shared__ uint32_t total[2];
+    __shared__ uint32_t flags_s;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int i = tid; i < 128; i += kPlanThreads) cnt[i] = 0;
+    if (tid == 0) flags_s = 0;
     __syncthreads();
     int32_t* lists[2] = {plan_short_list(ws, batch), plan_long_list(ws)};
-    for (int32_t b = tid; b < batch; b += blockDim.x) {
-        int32_t L = seq_lens[b];
-        L = L < 0 ? 0 : (L > max_seq_len ? max_seq_len : L);
-        const int cls = L > threshold ? 1 : 0;
-        const uint32_t pos = atomicAdd(&cur[cls][length_bucket(L)], 1u);
-        lists[cls][pos] = b;
+    uint32_t flags = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int32_t base = 0; base < batch; base += kPlanThreads * kPlanPerThread) {
+            int32_t len[kPlanPerThread];
+#pragma unroll
+            for (int q = 0; q < kPlanPerThread; ++q) {
+                const int32_t b = base + q * kPlanThreads + tid;
+                len[q] = b < batch ? __ldg(seq_lens + b) : 0;
+            }
+#pragma unroll
+            for (int q = 0; q < kPlanPerThread; ++q) {
+                const int32_t b = base + q * kPlanThreads + tid;
+                const bool valid = b < batch;
+                const int32_t L = clamp_len(len[q], max_seq_len, &flags);
+                const uint32_t key = valid ? static_cast<uint32_t>((L > threshold ? 64 : 0) + length_bucket(L)) : 255u;
+                const uint32_t peers = __match_any_sync(kFull, key);
+                const int leader = __ffs(peers) - 1;
+                uint32_t pos = 0;
+                if (lane == leader && valid) {
+                    if (pass == 0)
+                        atomicAdd(&cnt[key], __popc(peers));
+                    else
+                        pos = atomicAdd(&cur[key], __popc(peers));
+                }
+                if (pass == 1) {
+                    pos = __shfl_sync(kFull, pos, leader) + __popc(peers & lt_mask);
+                    if (valid) lists[key >> 6][pos] = b;
+                }
+            }
+        }
+        if (pass == 0) {
+            if (flags) atomicOr(&flags_s, flags);
+            __syncthreads();
+            if (tid < 2) {  // exclusive offsets within each class, longest bucket first
+                uint32_t run = 0;
+                for (int k = 63; k >= 0; --k) {
+                    cur[tid * 64 + k] = run;
+                    run += cnt[tid * 64 + k];
+                }
+                total[tid] = run;
+            }
+            __syncthreads();
+        }
     }
     if (tid == 0) {
         PlanHeader* h = static_cast<PlanHeader*>(ws);
@@ -961,9 +1010,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* seq_lens, int
         h->batch = batch;
         h->max_seq_len = max_seq_len;
         h->long_threshold = threshold;
-        h->n_long = static_cast<int32_t>(cnt[1][0]);
-        h->n_short = static_cast<int32_t>(cnt[0][0]);
-        h->flags = flags;
+        h->n_long = static_cast<int32_t>(total[1]);
+        h->n_short = static_cast<int32_t>(total[0]);
+        h->flags = flags_s;
     }
 }
 
@@ -1097,7 +1146,7 @@ cudaError_t select_occupancy(int cluster, size_t smem, int* units_out) {
 
 cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
                         void* workspace, cudaStream_t stream) {
-    return launch_plain(plan_kernel, dim3(1), dim3(1024), stream, seq_lens, batch, max_seq_len, long_threshold,
+    return launch_plain(plan_kernel, dim3(1), dim3(kPlanThreads), stream, seq_lens, batch, max_seq_len, long_threshold,
                         workspace);
 }
 

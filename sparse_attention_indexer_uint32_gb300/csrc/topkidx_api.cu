@@ -75,28 +75,36 @@ struct PathConfig {
     size_t smem;
 };
 
-PathConfig path_config(int cluster, int32_t k, const topk_tuning_t& t) {
+int sm_count() {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+// Launch shape of the select kernel.  Single blocks: a 4 x 8 KB ring and a
+// candidate buffer of 4k entries (>= 2048), which fits 3 blocks per SM at
+// k = 512.  Clusters: a 6 x 8 KB ring (two blocks per SM) when the long rows
+// can fill the GPU, and a 16 x 8 KB ring when they cannot (few rows: each SM
+// then has to keep more bytes in flight on its own).
+PathConfig path_config(int cluster, int32_t k, int32_t batch, const topk_tuning_t& t) {
     PathConfig c;
     c.cluster = cluster;
-    const int nt = select_threads(cluster);
-    if (cluster == 1) {
-        c.tile = 2048;
+    c.tile = 2048;
+    if (cluster == 1)
         c.stages = 4;
-    } else {
-        c.tile = 2048;
-        c.stages = 4;
-    }
+    else
+        c.stages = static_cast<int64_t>(batch) * cluster * 2 <= sm_count() ? 16 : 6;
     int cap = t.candidate_capacity;
     if (cap == 0) {
-        cap = cluster == 1 ? 4 * k : 2 * k;
+        cap = cluster == 1 ? 4 * k : k;
         if (cap < 2048) cap = 2048;
         if (cap > 16384) cap = 16384;
         cap = (cap + 63) / 64 * 64;
     }
     c.cap = cap;
     int samples = t.samples;
-    if (samples == 0) samples = kSamplesPerThread * nt;
-    if (samples > kSamplesPerThread * nt) samples = kSamplesPerThread * nt;
+    if (samples == 0 || samples > kMaxSamples) samples = kMaxSamples;
     c.samples = samples;
     c.smem = make_layout(cluster, c.tile, c.stages, c.cap, k).total;
     return c;
@@ -165,7 +173,8 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (t->candidate_capacity != 0 &&
         (t->candidate_capacity < 2048 || t->candidate_capacity > 16384 || t->candidate_capacity % 64 != 0))
         return TOPK_EINVAL;
-    if (t->samples != 0 && (t->samples < 32 || t->samples > 4096 || t->samples % 32 != 0)) return TOPK_EINVAL;
+    if (t->samples != 0 && (t->samples < 32 || t->samples > kMaxSamples || t->samples % 32 != 0))
+        return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -231,7 +240,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
 
     const bool launch_long = max_seq_len > threshold;
     if (launch_long) {
-        const PathConfig c = path_config(t.cluster_size, k, t);
+        const PathConfig c = path_config(t.cluster_size, k, batch, t);
         int units = 0;
         const topk_status_t r = resident_units(c.cluster, c.smem, &units);
         if (r != TOPK_OK) return r;
@@ -247,7 +256,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
     }
     {
-        const PathConfig c = path_config(1, k, t);
+        const PathConfig c = path_config(1, k, batch, t);
         int units = 0;
         const topk_status_t r = resident_units(1, c.smem, &units);
         if (r != TOPK_OK) return r;
