@@ -84,6 +84,30 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
     return v;
 }
 
+// Reserves consecutive slots of a shared-memory list for the lanes whose
+// `flag` is set, with a single atomic per warp, and returns this lane's slot
+// (meaningful only where `flag`).  Every lane of the warp must call it.
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, bool flag, int lane) {
+    const uint32_t m = __ballot_sync(kFull, flag);
+    if (m == 0u) return 0u;
+    const int leader = __ffs(m) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
+    base = __shfl_sync(kFull, base, leader);
+    return base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+}
+
+// Reserves `n` consecutive slots per lane (lane order) with a single atomic
+// per warp; returns this lane's first slot.  Every lane must call it.
+__device__ __forceinline__ uint32_t warp_reserve_n(uint32_t* counter, uint32_t n, int lane) {
+    const uint32_t incl = warp_inclusive_sum(n, lane);
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && total != 0u) base = atomicAdd(counter, total);
+    base = __shfl_sync(kFull, base, 31);
+    return base + incl - n;
+}
+
 __device__ __forceinline__ int32_t page_map(const int32_t* pt_row, int32_t log2_page, int32_t raw) {
     if (raw < 0) return -1;
     const uint32_t page = static_cast<uint32_t>(__ldg(pt_row + (raw >> log2_page)));
@@ -255,7 +279,7 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
 //     cluster_threshold": the transform is a separate pass).
 // ============================================================================
 template <int NT, int C>
-__global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
+__global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const SelectParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Layout lay = make_layout(C, p.tile, p.stages, p.cap, p.k);
     Smem s;
@@ -276,6 +300,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
     s.empty = s.full + p.stages;
 
     constexpr int kSamplesPerThread = kMaxSamples / NT;
+    constexpr int kVecPerStep = 2;  // float4s per thread per reservation step
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = (C > 1) ? ptx::cluster_ctarank() : 0u;
     const uint32_t unit = (C > 1) ? ptx::cluster_id_x() : blockIdx.x;
@@ -295,7 +320,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
 
     const uint32_t K = static_cast<uint32_t>(p.k);
     const uint32_t cap = static_cast<uint32_t>(p.cap);
-    const uint32_t tile = static_cast<uint32_t>(p.tile);
+    const uint32_t tile = static_cast<uint32_t>(p.tile);  // a multiple of 4 * kVecPerStep * NT floats
+    const uint32_t vec_per_tile = tile / (4u * NT);       // float4s per thread per bulk-copy tile
     const uint32_t stages = static_cast<uint32_t>(p.stages);
 
     // ---------------------------------------------------------------- init
@@ -536,25 +562,44 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                 const uint32_t nvec = min(tile, n4 - off) >> 2;
                 const float4* v4 = reinterpret_cast<const float4*>(s.ring + static_cast<size_t>(st) * tile);
                 const uint32_t base_idx = s0 + off;
-                for (uint32_t v = tid; v < nvec; v += NT) {
-                    const float4 x = v4[v];
+                // Each thread takes kVecPerTile float4s of the tile (consecutive
+                // threads on consecutive float4s), keeps their keys in registers,
+                // counts the gated ones in the histogram and reserves their buffer
+                // slots with one warp-wide reservation per tile.
+#pragma unroll 1
+                for (uint32_t q0 = 0; q0 < vec_per_tile; q0 += kVecPerStep) {
+                uint32_t keys[4 * kVecPerStep];
+                uint32_t gmask = 0;
+#pragma unroll
+                for (int q = 0; q < kVecPerStep; ++q) {
+                    const uint32_t v = (q0 + q) * NT + tid;
+                    const bool in = v < nvec;
+                    const float4 x = in ? v4[v] : make_float4(0.f, 0.f, 0.f, 0.f);
                     const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint32_t idx = base_idx + 4u * v + c;
                         const uint32_t key = score_key(xs[c]);
-                        if (key >= lo && idx < s1) {
-                            const uint32_t bin = min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1));
-                            atomicAdd(&s.hist_a[bin], 1u);
-                            if (buffering) {
-                                const uint32_t slot = atomicAdd(&s.ctl->ncand, 1u);
-                                if (slot < cap) {
-                                    s.cand_key[slot] = key;
-                                    s.cand_idx[slot] = idx;
-                                }
-                            }
+                        keys[4 * q + c] = key;
+                        const bool gated = in && key >= lo && base_idx + 4u * v + c < s1;
+                        if (gated) {
+                            atomicAdd(&s.hist_a[min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1))], 1u);
+                            gmask |= 1u << (4 * q + c);
                         }
                     }
+                }
+                if (buffering) {
+                    uint32_t slot = warp_reserve_n(&s.ctl->ncand, __popc(gmask), lane);
+#pragma unroll
+                    for (int e = 0; e < 4 * kVecPerStep; ++e) {
+                        if (gmask >> e & 1u) {
+                            if (slot < cap) {
+                                s.cand_key[slot] = keys[e];
+                                s.cand_idx[slot] = base_idx + 4u * ((q0 + (e >> 2)) * NT + tid) + (e & 3);
+                            }
+                            ++slot;
+                        }
+                    }
+                }
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&s.empty[st]);
@@ -602,12 +647,44 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
             const uint32_t nvec_slice = n4_slice >> 2;
             const float4* slice4 = reinterpret_cast<const float4*>(row_ptr + s0);
 
-            auto emit_push = [&](uint32_t idx) {
-                const uint32_t slot = atomicAdd(&s.ctl->nemit, 1u);
-                if (slot < K)
-                    s.emit[slot] = idx;
-                else
-                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+            // Appends `idx` to the emit list for the lanes with `flag`; every lane
+            // of the warp must call it.
+            auto emit_warp = [&](bool flag, uint32_t idx) {
+                const uint32_t slot = warp_reserve(&s.ctl->nemit, flag, lane);
+                if (flag) {
+                    if (slot < K)
+                        s.emit[slot] = idx;
+                    else
+                        atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                }
+            };
+            // Emits the positions of the buffer entries that satisfy `take(key,
+            // position)`: each thread reads 4 entries per step, one warp-wide
+            // reservation per step.
+            auto emit_from_buffer = [&](uint32_t nc, auto take) {
+                for (uint32_t i0 = 0; i0 < nc; i0 += 4u * NT) {
+                    uint32_t pos[4];
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t i = i0 + q * NT + tid;
+                        const bool in = i < nc;
+                        const uint32_t key = in ? s.cand_key[i] : 0u;
+                        pos[q] = in ? s.cand_idx[i] : 0u;
+                        if (in && take(key, pos[q])) m |= 1u << q;
+                    }
+                    uint32_t slot = warp_reserve_n(&s.ctl->nemit, __popc(m), lane);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (m >> q & 1u) {
+                            if (slot < K)
+                                s.emit[slot] = pos[q];
+                            else
+                                atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                            ++slot;
+                        }
+                    }
+                }
             };
 
             for (int round = 0;; ++round) {
@@ -622,24 +699,25 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                     __syncthreads();
                     if (tid == 0) s.ctl->ncand = 0;
                     __syncthreads();
-                    for (uint32_t v = tid; v < nvec_slice; v += NT) {
-                        const float4 x = __ldg(slice4 + v);
+                    for (uint32_t v0 = warp * 32u; v0 < nvec_slice; v0 += NT) {
+                        const uint32_t v = v0 + lane;
+                        const bool in = v < nvec_slice;
+                        const float4 x = in ? __ldg(slice4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                         const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const uint32_t idx = s0 + 4u * v + c;
                             const uint32_t key = score_key(xs[c]);
-                            if (idx < s1 && key >= r_lo) {
-                                if (key > r_hi) {
-                                    emit_push(idx);
+                            const bool live = in && idx < s1;
+                            emit_warp(live && key > r_hi, idx);
+                            const bool keep = live && key >= r_lo && key <= r_hi;
+                            const uint32_t slot = warp_reserve(&s.ctl->ncand, keep, lane);
+                            if (keep) {
+                                if (slot < cap) {
+                                    s.cand_key[slot] = key;
+                                    s.cand_idx[slot] = idx;
                                 } else {
-                                    const uint32_t slot = atomicAdd(&s.ctl->ncand, 1u);
-                                    if (slot < cap) {
-                                        s.cand_key[slot] = key;
-                                        s.cand_idx[slot] = idx;
-                                    } else {
-                                        atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
-                                    }
+                                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
                                 }
                             }
                         }
@@ -711,10 +789,7 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                 const bool all_eq = (quota == local_cnt);
                 if (!stream_mode) {
                     const uint32_t nc = s.ctl->ncand;
-                    for (uint32_t i = tid; i < nc; i += NT) {
-                        const uint32_t key = s.cand_key[i];
-                        if (key > T || (all_eq && key == T)) emit_push(s.cand_idx[i]);
-                    }
+                    emit_from_buffer(nc, [&](uint32_t key, uint32_t) { return key > T || (all_eq && key == T); });
                     if (!all_eq && quota > 0) {
                         // The `quota` smallest positions among this block's copies of T:
                         // rounds on v = ~position (larger v = smaller position).
@@ -742,16 +817,18 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                         // Above the final range: taken.  Inside it: a warp sort picks the rest.
                         if (tid == 0) s.ctl->nfin = 0;
                         __syncthreads();
-                        for (uint32_t i = tid; i < nc; i += NT) {
-                            if (s.cand_key[i] != T) continue;
-                            const uint32_t v = ~s.cand_idx[i];
-                            if (v > v_hi) {
-                                emit_push(s.cand_idx[i]);
-                            } else if (v >= v_lo) {
-                                const uint32_t slot = atomicAdd(&s.ctl->nfin, 1u);
+                        for (uint32_t i0 = warp * 32u; i0 < nc; i0 += NT) {
+                            const uint32_t i = i0 + lane;
+                            const bool eq = i < nc && s.cand_key[i] == T;
+                            const uint32_t pos = eq ? s.cand_idx[i] : 0u;
+                            const uint32_t v = ~pos;
+                            emit_warp(eq && v > v_hi, pos);
+                            const bool fin = eq && v >= v_lo && v <= v_hi;
+                            const uint32_t slot = warp_reserve(&s.ctl->nfin, fin, lane);
+                            if (fin) {
                                 if (slot < static_cast<uint32_t>(kFinish)) {
                                     s.fin_key[slot] = v;
-                                    s.fin_idx[slot] = s.cand_idx[i];
+                                    s.fin_idx[slot] = pos;
                                 } else {
                                     atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
                                 }
@@ -765,8 +842,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                                                    : 0ull;
                             const uint64_t srt = warp_sort_desc(e, lane);
                             const uint32_t take = quota - v_g;
-                            if (static_cast<uint32_t>(lane) < take && srt != 0ull)
-                                emit_push(~static_cast<uint32_t>(srt >> 32));
+                            emit_warp(static_cast<uint32_t>(lane) < take && srt != 0ull,
+                                      ~static_cast<uint32_t>(srt >> 32));
                         }
                     }
                 } else {
@@ -777,25 +854,20 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                     for (uint32_t vb = 0; vb < nvec_slice; vb += NT) {
                         const uint32_t v = vb + tid;
                         uint32_t eqm = 0;
-                        if (v < nvec_slice) {
-                            const float4 x = __ldg(slice4 + v);
-                            const float xs[4] = {x.x, x.y, x.z, x.w};
+                        const bool in = v < nvec_slice;
+                        const float4 x = in ? __ldg(slice4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const uint32_t idx = s0 + 4u * v + c;
-                                const uint32_t key = score_key(xs[c]);
-                                if (idx < s1) {
-                                    if (key > T)
-                                        emit_push(idx);
-                                    else if (key == T)
-                                        eqm |= 1u << c;
-                                }
-                            }
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t idx = s0 + 4u * v + c;
+                            const uint32_t key = score_key(xs[c]);
+                            const bool live = in && idx < s1;
+                            emit_warp(live && key > T, idx);
+                            if (live && key == T) eqm |= 1u << c;
                         }
                         if (!ordered) {
-                            if (all_eq)
-                                for (int c = 0; c < 4; ++c)
-                                    if (eqm >> c & 1u) emit_push(s0 + 4u * v + c);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) emit_warp(all_eq && (eqm >> c & 1u), s0 + 4u * v + c);
                             continue;
                         }
                         const uint32_t n_eq = __popc(eqm);
@@ -809,11 +881,11 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                             tot += t;
                         }
                         uint32_t r0 = running + pre + incl - n_eq;
+#pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            if (eqm >> c & 1u) {
-                                if (r0 < quota) emit_push(s0 + 4u * v + c);
-                                ++r0;
-                            }
+                            const bool e = (eqm >> c & 1u) != 0u;
+                            emit_warp(e && r0 < quota, s0 + 4u * v + c);
+                            r0 += e ? 1u : 0u;
                         }
                         running += tot;
                         __syncthreads();
@@ -825,11 +897,10 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                 const uint32_t fin_nfin = ptx::smem_addr(&s.ctl->nfin);
                 const uint32_t fin_key0 = ptx::smem_addr(s.fin_key);
                 const uint32_t fin_idx0 = ptx::smem_addr(s.fin_idx);
+                emit_from_buffer(nc, [&](uint32_t key, uint32_t) { return key > r_hi; });
                 for (uint32_t i = tid; i < nc; i += NT) {
                     const uint32_t key = s.cand_key[i];
-                    if (key > r_hi) {
-                        emit_push(s.cand_idx[i]);
-                    } else if (key >= r_lo) {
+                    if (key >= r_lo && key <= r_hi) {
                         if (C > 1) {
                             const uint32_t slot = ptx::atom_add_cluster_u32(ptx::map_rank(fin_nfin, 0), 1u);
                             if (slot < static_cast<uint32_t>(kFinish)) {
@@ -859,8 +930,8 @@ __global__ void __launch_bounds__(NT) select_kernel(const SelectParams p) {
                                            ? (static_cast<uint64_t>(s.fin_key[lane]) << 32) | (~s.fin_idx[lane])
                                            : 0ull;
                     const uint64_t srt = warp_sort_desc(e, lane);
-                    if (static_cast<uint32_t>(lane) < need && srt != 0ull)
-                        emit_push(~static_cast<uint32_t>(srt & 0xffffffffull));
+                    emit_warp(static_cast<uint32_t>(lane) < need && srt != 0ull,
+                              ~static_cast<uint32_t>(srt & 0xffffffffull));
                 }
             }
             __syncthreads();
@@ -971,6 +1042,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
             }
 #pragma unroll
             for (int q = 0; q < kPlanPerThread; ++q) {
+                if (base + q * kPlanThreads >= batch) break;  // the same for the whole block
                 const int32_t b = base + q * kPlanThreads + tid;
                 const bool valid = b < batch;
                 const int32_t L = clamp_len(len[q], max_seq_len, &flags);

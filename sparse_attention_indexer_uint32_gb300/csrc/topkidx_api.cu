@@ -82,19 +82,18 @@ int sm_count() {
     return sms > 0 ? sms : 1;
 }
 
-// Launch shape of the select kernel.  Single blocks: a 4 x 8 KB ring and a
-// candidate buffer of 4k entries (>= 2048), which fits 3 blocks per SM at
-// k = 512.  Clusters: a 6 x 8 KB ring (two blocks per SM) when the long rows
-// can fill the GPU, and a 16 x 8 KB ring when they cannot (few rows: each SM
-// then has to keep more bytes in flight on its own).
+// Launch shape of the select kernel.  Bulk copies are 16 KB (32 KB when few
+// cluster rows must each pull more bytes per SM): smaller copies cost more
+// per byte.  Single blocks: a 2-stage ring and a candidate buffer of 4k
+// entries (>= 2048), 3 blocks per SM at k = 512.  Clusters: 3 x 16 KB (two
+// blocks per SM) when the long rows can fill the GPU, 5 x 32 KB when they
+// cannot.
 PathConfig path_config(int cluster, int32_t k, int32_t batch, const topk_tuning_t& t) {
     PathConfig c;
     c.cluster = cluster;
-    c.tile = 2048;
-    if (cluster == 1)
-        c.stages = 4;
-    else
-        c.stages = static_cast<int64_t>(batch) * cluster * 2 <= sm_count() ? 16 : 6;
+    const bool few_rows = cluster > 1 && static_cast<int64_t>(batch) * cluster * 2 <= sm_count();
+    c.tile = few_rows ? 8192 : 4096;  // floats per bulk copy: 32 KB or 16 KB
+    c.stages = cluster == 1 ? 2 : (few_rows ? 5 : 3);
     int cap = t.candidate_capacity;
     if (cap == 0) {
         cap = cluster == 1 ? 4 * k : k;
