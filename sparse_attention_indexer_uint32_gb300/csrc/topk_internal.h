@@ -89,7 +89,7 @@ struct __align__(16) Control {
 
 struct Layout {
     uint32_t ring, hist_a, hist_b, hist_m, cand_key, cand_idx, emit, fin_key, fin_idx, warp_tot, ctl;
-    uint32_t items_row, items_len, mbar, total;
+    uint32_t items_row, items_len, items_tiles, mbar, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -122,6 +122,8 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
     l.items_row = o;
     o += kItemsMax * 4u;
     l.items_len = o;
+    o += kItemsMax * 4u;
+    l.items_tiles = o;
     o += kItemsMax * 4u;
     l.mbar = align_up(o, 8);
     o = l.mbar + 2u * stages * 8u;

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstddef>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -87,23 +88,23 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
 // Reserves consecutive slots of a shared-memory list for the lanes whose
 // `flag` is set, with a single atomic per warp, and returns this lane's slot
 // (meaningful only where `flag`).  Every lane of the warp must call it.
-__device__ __forceinline__ uint32_t warp_reserve(uint32_t* counter, bool flag, int lane) {
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t counter, bool flag, int lane) {
     const uint32_t m = __ballot_sync(kFull, flag);
     if (m == 0u) return 0u;
     const int leader = __ffs(m) - 1;
     uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
+    if (lane == leader) base = ptx::atom_add_s(counter, static_cast<uint32_t>(__popc(m)));
     base = __shfl_sync(kFull, base, leader);
     return base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
 }
 
 // Reserves `n` consecutive slots per lane (lane order) with a single atomic
 // per warp; returns this lane's first slot.  Every lane must call it.
-__device__ __forceinline__ uint32_t warp_reserve_n(uint32_t* counter, uint32_t n, int lane) {
+__device__ __forceinline__ uint32_t warp_reserve_n(uint32_t counter, uint32_t n, int lane) {
     const uint32_t incl = warp_inclusive_sum(n, lane);
     const uint32_t total = __shfl_sync(kFull, incl, 31);
     uint32_t base = 0;
-    if (lane == 31 && total != 0u) base = atomicAdd(counter, total);
+    if (lane == 31 && total != 0u) base = ptx::atom_add_s(counter, total);
     base = __shfl_sync(kFull, base, 31);
     return base + incl - n;
 }
@@ -120,27 +121,21 @@ struct ScanResult {
     uint32_t local;  // this block's own count in `bin` (differs from `count` only in a cluster)
 };
 
+// 32-bit shared-window addresses of the block's shared-memory regions.
 struct Smem {
-    float* ring;
-    uint32_t* hist_a;
-    uint32_t* hist_b;
-    uint32_t* hist_m;
-    uint32_t* cand_key;
-    uint32_t* cand_idx;
-    uint32_t* emit;
-    uint32_t* fin_key;
-    uint32_t* fin_idx;
-    uint32_t* warp_tot;
-    Control* ctl;
-    int32_t* it_row;
-    int32_t* it_len;
+    uint32_t ring, hist_a, hist_b, hist_m, cand_key, cand_idx, emit, fin_key, fin_idx, warp_tot, ctl;
+    uint32_t it_row, it_len, it_tiles;
     uint64_t* full;
     uint64_t* empty;
+    Control* ctl_ptr;
 };
 
+// Addresses of Control fields.
+#define CTL(s, field) ((s).ctl + static_cast<uint32_t>(offsetof(Control, field)))
+
 template <int NT>
-__device__ __forceinline__ void clear_hist(uint32_t* h, int tid) {
-    for (int i = tid * 4; i < kBinsX; i += NT * 4) *reinterpret_cast<uint4*>(h + i) = make_uint4(0, 0, 0, 0);
+__device__ __forceinline__ void clear_hist(uint32_t h, int tid) {
+    for (int i = tid * 4; i < kBinsX; i += NT * 4) ptx::sts_u4(h + 4u * i, make_uint4(0, 0, 0, 0));
 }
 
 // Finds, in a histogram whose bins are ordered by key, the bin where the
@@ -148,9 +143,11 @@ __device__ __forceinline__ void clear_hist(uint32_t* h, int tid) {
 // count in the bins above it, its own count and the histogram total.  If the
 // total is below `need`, bin is 0xffffffff.  Every thread of the block must
 // call it; it contains two block barriers and reads `h` before the first.
+// `h_local` (0: same as `h`) is the block's own histogram, whose count of
+// the found bin is returned as `local`.
 template <int NT>
-__device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need, int tid,
-                                const uint32_t* h_local = nullptr) {
+__device__ __forceinline__ ScanResult scan_find(const Smem& s, uint32_t h, uint32_t need, int tid,
+                                                uint32_t h_local = 0) {
     constexpr int BPT = kBins / NT;
     static_assert(BPT == 4 || BPT == 8, "bins per thread");
     const int lane = tid & 31, warp = tid >> 5;
@@ -158,7 +155,7 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
     uint32_t v[BPT];
 #pragma unroll
     for (int i = 0; i < BPT; i += 4) {
-        const uint4 q = *reinterpret_cast<const uint4*>(h + base + i);
+        const uint4 q = ptx::lds_u4(h + 4u * (base + i));
         v[i] = q.x;
         v[i + 1] = q.y;
         v[i + 2] = q.z;
@@ -168,15 +165,19 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
 #pragma unroll
     for (int i = 0; i < BPT; ++i) sum += v[i];
     const uint32_t incl = warp_inclusive_sum(sum, lane);
-    if (lane == 31) s.warp_tot[warp] = incl;
-    if (tid == 0) s.ctl->res_bin = 0xffffffffu;
+    if (lane == 31) ptx::sts_u32(s.warp_tot + 4u * warp, incl);
+    if (tid == 0) ptx::sts_u32(CTL(s, res_bin), 0xffffffffu);
     __syncthreads();
     uint32_t pre = 0, total = 0;
 #pragma unroll
-    for (int w = 0; w < NT / 32; ++w) {
-        const uint32_t t = s.warp_tot[w];
-        pre += (w < warp) ? t : 0u;
-        total += t;
+    for (int w = 0; w < NT / 32; w += 4) {
+        const uint4 t = ptx::lds_u4(s.warp_tot + 4u * w);
+        const uint32_t ts[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            pre += (w + u < warp) ? ts[u] : 0u;
+            total += ts[u];
+        }
     }
     const uint32_t excl = pre + incl - sum;
     if (need > excl && need <= excl + sum) {
@@ -184,10 +185,10 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
 #pragma unroll
         for (int i = BPT - 1; i >= 0; --i) {
             if (acc + v[i] >= need) {
-                s.ctl->res_bin = static_cast<uint32_t>(base + i);
-                s.ctl->res_above = acc;
-                s.ctl->res_count = v[i];
-                s.ctl->res_local = h_local ? h_local[base + i] : v[i];
+                ptx::sts_u32(CTL(s, res_bin), static_cast<uint32_t>(base + i));
+                ptx::sts_u32(CTL(s, res_above), acc);
+                ptx::sts_u32(CTL(s, res_count), v[i]);
+                ptx::sts_u32(CTL(s, res_local), h_local ? ptx::lds_u32(h_local + 4u * (base + i)) : v[i]);
                 break;
             }
             acc += v[i];
@@ -195,10 +196,10 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
     }
     __syncthreads();
     ScanResult r;
-    r.bin = s.ctl->res_bin;
-    r.above = s.ctl->res_above;
-    r.count = s.ctl->res_count;
-    r.local = s.ctl->res_local;
+    r.bin = ptx::lds_u32(CTL(s, res_bin));
+    r.above = ptx::lds_u32(CTL(s, res_above));
+    r.count = ptx::lds_u32(CTL(s, res_count));
+    r.local = ptx::lds_u32(CTL(s, res_local));
     r.total = total;
     return r;
 }
@@ -211,12 +212,12 @@ __device__ ScanResult scan_find(const Smem& s, const uint32_t* h, uint32_t need,
 // all-gather, both through distributed shared memory.  The caller must have
 // finished writing `h_local` (all threads reach the first cluster barrier).
 template <int NT, int C>
-__device__ void cluster_merge(const Smem& s, uint32_t* h_local, uint32_t rank, int tid) {
+__device__ __forceinline__ void cluster_merge(const Smem& s, uint32_t h_local, uint32_t rank, int tid) {
     ptx::cluster_sync();
     constexpr int chunk = kBinsX / C;
     static_assert(chunk % 4 == 0, "merge chunk must be whole uint4s");
-    const uint32_t lbase = ptx::smem_addr(h_local) + rank * chunk * 4u;
-    const uint32_t mbase = ptx::smem_addr(s.hist_m) + rank * chunk * 4u;
+    const uint32_t lbase = h_local + rank * chunk * 4u;
+    const uint32_t mbase = s.hist_m + rank * chunk * 4u;
     for (int i = tid * 4; i < chunk; i += NT * 4) {
         uint4 acc = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -254,12 +255,13 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
 //
 // Per row:
 //  1. Gate.  Up to `samples` scores of the row are read (prefetched while the
-//     previous row is processed).  Their keys give a lower bound `lo` that
-//     about 2*k elements of the row exceed (the sample's r-th largest key,
-//     r = 2*E + 8 with E the expected number of samples in the top k) and a
-//     bin width so that the sampled range covers about 1024 of the 2048 bins
-//     (the "linear mapping" of the DistRadixTopK README: bins spread over the
-//     range where the threshold lies, so few elements share its bin).
+//     previous row is processed).  Their keys give a lower bound `lo`: the
+//     sample's r-th largest key, r = max(E + 4 sqrt(E) + 4, the rank that
+//     fills half the candidate buffer), E the expected number of samples in
+//     the top k.  The bin width is chosen so that the sampled range covers
+//     about 1024 of the 2048 bins (the "linear mapping" of the DistRadixTopK
+//     README: bins spread over the range where the threshold lies, so few
+//     elements share its bin).
 //  2. Pass 1 streams the slice through the bulk-copy ring: every element with
 //     key >= lo is counted in the histogram and pushed (key, position) into a
 //     candidate buffer in shared memory.  In a cluster the histograms are
@@ -282,22 +284,25 @@ template <int NT, int C>
 __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const SelectParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Layout lay = make_layout(C, p.tile, p.stages, p.cap, p.k);
+    const uint32_t sbase = ptx::smem_addr(smem_raw);
     Smem s;
-    s.ring = reinterpret_cast<float*>(smem_raw + lay.ring);
-    s.hist_a = reinterpret_cast<uint32_t*>(smem_raw + lay.hist_a);
-    s.hist_b = reinterpret_cast<uint32_t*>(smem_raw + lay.hist_b);
-    s.hist_m = reinterpret_cast<uint32_t*>(smem_raw + lay.hist_m);
-    s.cand_key = reinterpret_cast<uint32_t*>(smem_raw + lay.cand_key);
-    s.cand_idx = reinterpret_cast<uint32_t*>(smem_raw + lay.cand_idx);
-    s.emit = reinterpret_cast<uint32_t*>(smem_raw + lay.emit);
-    s.fin_key = reinterpret_cast<uint32_t*>(smem_raw + lay.fin_key);
-    s.fin_idx = reinterpret_cast<uint32_t*>(smem_raw + lay.fin_idx);
-    s.warp_tot = reinterpret_cast<uint32_t*>(smem_raw + lay.warp_tot);
-    s.ctl = reinterpret_cast<Control*>(smem_raw + lay.ctl);
-    s.it_row = reinterpret_cast<int32_t*>(smem_raw + lay.items_row);
-    s.it_len = reinterpret_cast<int32_t*>(smem_raw + lay.items_len);
+    s.ring = sbase + lay.ring;
+    s.hist_a = sbase + lay.hist_a;
+    s.hist_b = sbase + lay.hist_b;
+    s.hist_m = sbase + lay.hist_m;
+    s.cand_key = sbase + lay.cand_key;
+    s.cand_idx = sbase + lay.cand_idx;
+    s.emit = sbase + lay.emit;
+    s.fin_key = sbase + lay.fin_key;
+    s.fin_idx = sbase + lay.fin_idx;
+    s.warp_tot = sbase + lay.warp_tot;
+    s.ctl = sbase + lay.ctl;
+    s.it_row = sbase + lay.items_row;
+    s.it_len = sbase + lay.items_len;
+    s.it_tiles = sbase + lay.items_tiles;
     s.full = reinterpret_cast<uint64_t*>(smem_raw + lay.mbar);
     s.empty = s.full + p.stages;
+    s.ctl_ptr = reinterpret_cast<Control*>(smem_raw + lay.ctl);
 
     constexpr int kSamplesPerThread = kMaxSamples / NT;
     constexpr int kVecPerStep = 2;  // float4s per thread per reservation step
@@ -331,9 +336,11 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             ptx::mbar_init(&s.empty[i], NT / 32);
         }
         ptx::fence_mbarrier_init();
-        Control* c = s.ctl;
-        c->ncand = c->nemit = c->nfin = c->smax = 0;
-        c->err = 0;
+        ptx::sts_u32(CTL(s, ncand), 0);
+        ptx::sts_u32(CTL(s, nemit), 0);
+        ptx::sts_u32(CTL(s, nfin), 0);
+        ptx::sts_u32(CTL(s, smax), 0);
+        ptx::sts_u32(CTL(s, err), 0);
     }
     clear_hist<NT>(s.hist_a, tid);
     clear_hist<NT>(s.hist_b, tid);
@@ -342,6 +349,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
 
     const uint64_t policy = ptx::l2_policy_evict_first();
     const uint32_t m_max = static_cast<uint32_t>(p.samples);
+    auto set_err = [&](uint32_t f) { atomicOr(&s.ctl_ptr->err, f); };
 
     // Producer state (meaningful in thread 0 only) and the consumer sequence.
     uint32_t pseq = 0, cseq = 0;
@@ -354,36 +362,34 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
         s0 = min(static_cast<uint32_t>(L), rank * chunk);
         s1 = min(static_cast<uint32_t>(L), s0 + chunk);
     };
-    auto tiles_of = [&](int32_t L) -> uint32_t {
-        if (L <= p.k) return 0u;
-        uint32_t s0, s1;
-        slice_of(L, s0, s1);
-        if (s1 <= s0) return 0u;
-        const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
-        return (n4 + tile - 1) / tile;
-    };
 
     for (int32_t w0 = 0; w0 < my_items; w0 += kItemsMax) {
         const int32_t nw = min(kItemsMax, my_items - w0);
         for (int32_t i = tid; i < nw; i += NT) {
             const int32_t it = static_cast<int32_t>(unit) + (w0 + i) * static_cast<int32_t>(nunits);
             const int32_t row = it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first];
+            int32_t L = -1;
+            uint32_t nt = 0;
             if (row < 0 || row >= p.batch) {  // a list that does not belong to this batch
                 atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
-                s.it_row[i] = 0;
-                s.it_len[i] = -1;
-                continue;
+            } else {
+                L = p.seq_lens[row];
+                if (L < 0) {
+                    atomicOr(p.flags, TOPK_FLAG_SEQ_NEGATIVE);
+                    L = 0;
+                } else if (L > p.max_seq_len) {
+                    atomicOr(p.flags, TOPK_FLAG_SEQ_CLAMPED);
+                    L = p.max_seq_len;
+                }
+                if (L > p.k) {  // rows with L <= k need no select, hence no tiles
+                    uint32_t s0, s1;
+                    slice_of(L, s0, s1);
+                    if (s1 > s0) nt = ((((s1 + 3u) & ~3u) - s0) + tile - 1) / tile;
+                }
             }
-            int32_t L = p.seq_lens[row];
-            if (L < 0) {
-                atomicOr(p.flags, TOPK_FLAG_SEQ_NEGATIVE);
-                L = 0;
-            } else if (L > p.max_seq_len) {
-                atomicOr(p.flags, TOPK_FLAG_SEQ_CLAMPED);
-                L = p.max_seq_len;
-            }
-            s.it_row[i] = row;
-            s.it_len[i] = L;
+            ptx::sts_u32(s.it_row + 4u * i, static_cast<uint32_t>(row < 0 || row >= p.batch ? 0 : row));
+            ptx::sts_u32(s.it_len + 4u * i, static_cast<uint32_t>(L));
+            ptx::sts_u32(s.it_tiles + 4u * i, nt);
         }
         __syncthreads();
         p_item = 0;
@@ -394,8 +400,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
         // is already free.
         auto pump = [&](uint32_t must) {
             while (p_item < nw && pseq < cseq + stages && !aborted) {
-                const int32_t L = s.it_len[p_item];
-                const uint32_t nt = tiles_of(L);
+                const uint32_t nt = ptx::lds_u32(s.it_tiles + 4u * p_item);
                 if (nt == 0) {
                     ++p_item;
                     p_tile = 0;
@@ -407,21 +412,23 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                     if (pseq <= must) {
                         if (!ptx::mbar_wait_bounded(&s.empty[st], par, p.timeout_ns)) {
                             aborted = true;
-                            atomicOr(&s.ctl->err, TOPK_FLAG_TIMEOUT);
+                            set_err(TOPK_FLAG_TIMEOUT);
                             break;
                         }
                     } else if (!ptx::mbar_test_wait(&s.empty[st], par)) {
                         break;
                     }
                 }
+                const int32_t L = static_cast<int32_t>(ptx::lds_u32(s.it_len + 4u * p_item));
                 uint32_t s0, s1;
                 slice_of(L, s0, s1);
                 const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
                 const uint32_t off = p_tile * tile;
                 const uint32_t elems = min(tile, n4 - off);
-                const float* src = p.scores + static_cast<int64_t>(s.it_row[p_item]) * p.row_stride + s0 + off;
+                const int32_t prow = static_cast<int32_t>(ptx::lds_u32(s.it_row + 4u * p_item));
+                const float* src = p.scores + static_cast<int64_t>(prow) * p.row_stride + s0 + off;
                 ptx::mbar_arrive_expect_tx(&s.full[st], elems * 4u);
-                ptx::bulk_copy_g2s(s.ring + static_cast<size_t>(st) * tile, src, elems * 4u, &s.full[st], policy);
+                ptx::bulk_copy_g2s_addr(s.ring + st * tile * 4u, src, elems * 4u, &s.full[st], policy);
                 ++pseq;
                 if (++p_tile == nt) {
                     ++p_item;
@@ -441,10 +448,11 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
 #pragma unroll
             for (int q = 0; q < kSamplesPerThread; ++q) smp[q] = 0.0f;
             if (j >= nw) return;
-            const int32_t L = s.it_len[j];
+            const int32_t L = static_cast<int32_t>(ptx::lds_u32(s.it_len + 4u * j));
             if (L <= p.k) return;
             const uint32_t M = samples_for(static_cast<uint32_t>(L));
-            const float* rowp = p.scores + static_cast<int64_t>(s.it_row[j]) * p.row_stride;
+            const float* rowp =
+                p.scores + static_cast<int64_t>(ptx::lds_u32(s.it_row + 4u * j)) * p.row_stride;
 #pragma unroll
             for (int q = 0; q < kSamplesPerThread; ++q) {
                 const uint32_t i = static_cast<uint32_t>(q * NT + tid);
@@ -454,8 +462,8 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
         load_samples(0);
 
         for (int32_t j = 0; j < nw; ++j) {
-            const int32_t row = s.it_row[j];
-            const int32_t L = s.it_len[j];
+            const int32_t row = static_cast<int32_t>(ptx::lds_u32(s.it_row + 4u * j));
+            const int32_t L = static_cast<int32_t>(ptx::lds_u32(s.it_len + 4u * j));
             if (L < 0) {  // rejected item: nothing to write
                 load_samples(j + 1);
                 continue;
@@ -480,14 +488,14 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
 
             uint32_t s0, s1;
             slice_of(L, s0, s1);
-            const uint32_t ntiles = tiles_of(L);
+            const uint32_t ntiles = ptx::lds_u32(s.it_tiles + 4u * j);
             const float* row_ptr = p.scores + static_cast<int64_t>(row) * p.row_stride;
 
             if (tid == 0) {
-                s.ctl->ncand = 0;
-                s.ctl->nemit = 0;
-                s.ctl->nfin = 0;
-                s.ctl->smax = 0;
+                ptx::sts_u32(CTL(s, ncand), 0);
+                ptx::sts_u32(CTL(s, nemit), 0);
+                ptx::sts_u32(CTL(s, nfin), 0);
+                ptx::sts_u32(CTL(s, smax), 0);
             }
             __syncthreads();
 
@@ -515,12 +523,12 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         const uint32_t i = static_cast<uint32_t>(q * NT + tid);
                         keys[q] = score_key(smp[q]);
                         if (i < M) {
-                            atomicAdd(&s.hist_a[keys[q] >> (32 - kBinBits)], 1u);
+                            ptx::red_add_s(s.hist_a + 4u * (keys[q] >> (32 - kBinBits)), 1u);
                             kmax = max(kmax, keys[q]);
                         }
                     }
                     kmax = __reduce_max_sync(kFull, kmax);
-                    if (lane == 0) atomicMax(&s.ctl->smax, kmax);
+                    if (lane == 0) atomicMax(&s.ctl_ptr->smax, kmax);
                     __syncthreads();
                     const ScanResult g = scan_find<NT>(s, s.hist_a, r, tid);
                     lo = g.bin << (32 - kBinBits);
@@ -530,7 +538,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         for (int q = 0; q < kSamplesPerThread; ++q) {
                             const uint32_t i = static_cast<uint32_t>(q * NT + tid);
                             if (i < M && (keys[q] >> (32 - kBinBits)) == g.bin)
-                                atomicAdd(&s.hist_b[(keys[q] >> (32 - 2 * kBinBits)) & (kBins - 1)], 1u);
+                                ptx::red_add_s(s.hist_b + 4u * ((keys[q] >> (32 - 2 * kBinBits)) & (kBins - 1)), 1u);
                         }
                         __syncthreads();
                         const ScanResult g2 = scan_find<NT>(s, s.hist_b, r - g.above, tid);
@@ -538,7 +546,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         clear_hist<NT>(s.hist_b, tid);
                     }
                     clear_hist<NT>(s.hist_a, tid);
-                    const uint32_t smax = s.ctl->smax;
+                    const uint32_t smax = ptx::lds_u32(CTL(s, smax));
                     const int b = bit_length(smax - lo);
                     shift = b > kBinBits - 1 ? b - (kBinBits - 1) : 0;
                     __syncthreads();
@@ -552,54 +560,55 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 if (tid == 0) pump(cseq);
                 __syncwarp();
                 const uint32_t st = cseq % stages;
-                const bool gave_up = (*reinterpret_cast<volatile uint32_t*>(&s.ctl->err) & TOPK_FLAG_TIMEOUT) != 0u;
+                const bool gave_up = (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) != 0u;
                 if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns)) {
-                    atomicOr(&s.ctl->err, TOPK_FLAG_TIMEOUT);
+                    set_err(TOPK_FLAG_TIMEOUT);
                     aborted = true;
                 }
                 const uint32_t off = t * tile;
                 const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
                 const uint32_t nvec = min(tile, n4 - off) >> 2;
-                const float4* v4 = reinterpret_cast<const float4*>(s.ring + static_cast<size_t>(st) * tile);
+                const uint32_t ring_st = s.ring + st * tile * 4u;
                 const uint32_t base_idx = s0 + off;
-                // Each thread takes kVecPerTile float4s of the tile (consecutive
-                // threads on consecutive float4s), keeps their keys in registers,
-                // counts the gated ones in the histogram and reserves their buffer
-                // slots with one warp-wide reservation per tile.
+                // Each thread takes float4s v = q * NT + tid of the tile, keeps their
+                // keys in registers, counts the gated ones in the histogram and
+                // reserves their buffer slots with one warp-wide reservation per step.
 #pragma unroll 1
                 for (uint32_t q0 = 0; q0 < vec_per_tile; q0 += kVecPerStep) {
-                uint32_t keys[4 * kVecPerStep];
-                uint32_t gmask = 0;
+                    uint32_t keys[4 * kVecPerStep];
+                    uint32_t gmask = 0;
 #pragma unroll
-                for (int q = 0; q < kVecPerStep; ++q) {
-                    const uint32_t v = (q0 + q) * NT + tid;
-                    const bool in = v < nvec;
-                    const float4 x = in ? v4[v] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float xs[4] = {x.x, x.y, x.z, x.w};
+                    for (int q = 0; q < kVecPerStep; ++q) {
+                        const uint32_t v = (q0 + q) * NT + tid;
+                        const bool in = v < nvec;
+                        const float4 x = in ? ptx::lds_f4(ring_st + 16u * v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t key = score_key(xs[c]);
-                        keys[4 * q + c] = key;
-                        const bool gated = in && key >= lo && base_idx + 4u * v + c < s1;
-                        if (gated) {
-                            atomicAdd(&s.hist_a[min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1))], 1u);
-                            gmask |= 1u << (4 * q + c);
-                        }
-                    }
-                }
-                if (buffering) {
-                    uint32_t slot = warp_reserve_n(&s.ctl->ncand, __popc(gmask), lane);
-#pragma unroll
-                    for (int e = 0; e < 4 * kVecPerStep; ++e) {
-                        if (gmask >> e & 1u) {
-                            if (slot < cap) {
-                                s.cand_key[slot] = keys[e];
-                                s.cand_idx[slot] = base_idx + 4u * ((q0 + (e >> 2)) * NT + tid) + (e & 3);
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t key = score_key(xs[c]);
+                            keys[4 * q + c] = key;
+                            const bool gated = in && key >= lo && base_idx + 4u * v + c < s1;
+                            if (gated) {
+                                ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
+                                               1u);
+                                gmask |= 1u << (4 * q + c);
                             }
-                            ++slot;
                         }
                     }
-                }
+                    if (buffering) {
+                        uint32_t slot = warp_reserve_n(CTL(s, ncand), __popc(gmask), lane);
+#pragma unroll
+                        for (int e = 0; e < 4 * kVecPerStep; ++e) {
+                            if (gmask >> e & 1u) {
+                                if (slot < cap) {
+                                    ptx::sts_u32(s.cand_key + 4u * slot, keys[e]);
+                                    ptx::sts_u32(s.cand_idx + 4u * slot,
+                                                 base_idx + 4u * ((q0 + (e >> 2)) * NT + tid) + (e & 3));
+                                }
+                                ++slot;
+                            }
+                        }
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&s.empty[st]);
@@ -608,14 +617,14 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             __syncthreads();
             if (tid == 0) pump(0);  // prefetch the next row while this one resolves
 
-            const uint32_t local_ovf = (!buffering || s.ctl->ncand > cap) ? 1u : 0u;
-            const uint32_t* hm = s.hist_a;
+            const uint32_t local_ovf = (!buffering || ptx::lds_u32(CTL(s, ncand)) > cap) ? 1u : 0u;
+            uint32_t hm = s.hist_a;
             if (C > 1) {
-                if (tid == 0) s.hist_a[kSlotOverflow] = local_ovf;
+                if (tid == 0) ptx::sts_u32(s.hist_a + 4u * kSlotOverflow, local_ovf);
                 cluster_merge<NT, C>(s, s.hist_a, rank, tid);
                 hm = s.hist_m;
             }
-            const bool overflow = (C > 1) ? (hm[kSlotOverflow] != 0u) : (local_ovf != 0u);
+            const bool overflow = (C > 1) ? (ptx::lds_u32(hm + 4u * kSlotOverflow) != 0u) : (local_ovf != 0u);
             ScanResult sr = scan_find<NT>(s, hm, Kp, tid, s.hist_a);
 
             // ----------------------------------------------------- 3. resolve
@@ -640,8 +649,8 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 local_cnt = sr.local;
             }
             clear_hist<NT>(s.hist_a, tid);
-            uint32_t* h_next = s.hist_b;
-            uint32_t* h_other = s.hist_a;
+            uint32_t h_next = s.hist_b;
+            uint32_t h_other = s.hist_a;
 
             const uint32_t n4_slice = (s1 > s0) ? ((s1 + 3u) & ~3u) - s0 : 0u;
             const uint32_t nvec_slice = n4_slice >> 2;
@@ -650,17 +659,17 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             // Appends `idx` to the emit list for the lanes with `flag`; every lane
             // of the warp must call it.
             auto emit_warp = [&](bool flag, uint32_t idx) {
-                const uint32_t slot = warp_reserve(&s.ctl->nemit, flag, lane);
+                const uint32_t slot = warp_reserve(CTL(s, nemit), flag, lane);
                 if (flag) {
                     if (slot < K)
-                        s.emit[slot] = idx;
+                        ptx::sts_u32(s.emit + 4u * slot, idx);
                     else
-                        atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                        set_err(TOPK_FLAG_INTERNAL);
                 }
             };
-            // Emits the positions of the buffer entries that satisfy `take(key,
-            // position)`: each thread reads 4 entries per step, one warp-wide
-            // reservation per step.
+            // Emits the positions of the buffer entries that satisfy `take(key)`:
+            // each thread reads 4 entries per step, one warp-wide reservation per
+            // step.
             auto emit_from_buffer = [&](uint32_t nc, auto take) {
                 for (uint32_t i0 = 0; i0 < nc; i0 += 4u * NT) {
                     uint32_t pos[4];
@@ -669,18 +678,18 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                     for (int q = 0; q < 4; ++q) {
                         const uint32_t i = i0 + q * NT + tid;
                         const bool in = i < nc;
-                        const uint32_t key = in ? s.cand_key[i] : 0u;
-                        pos[q] = in ? s.cand_idx[i] : 0u;
-                        if (in && take(key, pos[q])) m |= 1u << q;
+                        const uint32_t key = in ? ptx::lds_u32(s.cand_key + 4u * i) : 0u;
+                        pos[q] = in ? ptx::lds_u32(s.cand_idx + 4u * i) : 0u;
+                        if (in && take(key)) m |= 1u << q;
                     }
-                    uint32_t slot = warp_reserve_n(&s.ctl->nemit, __popc(m), lane);
+                    uint32_t slot = warp_reserve_n(CTL(s, nemit), __popc(m), lane);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if (m >> q & 1u) {
                             if (slot < K)
-                                s.emit[slot] = pos[q];
+                                ptx::sts_u32(s.emit + 4u * slot, pos[q]);
                             else
-                                atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                set_err(TOPK_FLAG_INTERNAL);
                             ++slot;
                         }
                     }
@@ -689,7 +698,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
 
             for (int round = 0;; ++round) {
                 if (round > 8) {
-                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                    set_err(TOPK_FLAG_INTERNAL);
                     break;
                 }
                 if (r_lo == r_hi) break;
@@ -697,7 +706,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 if (stream_mode && cnt <= cap) {
                     // Collect pass: emit everything above the bin, keep the bin.
                     __syncthreads();
-                    if (tid == 0) s.ctl->ncand = 0;
+                    if (tid == 0) ptx::sts_u32(CTL(s, ncand), 0);
                     __syncthreads();
                     for (uint32_t v0 = warp * 32u; v0 < nvec_slice; v0 += NT) {
                         const uint32_t v = v0 + lane;
@@ -711,13 +720,13 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                             const bool live = in && idx < s1;
                             emit_warp(live && key > r_hi, idx);
                             const bool keep = live && key >= r_lo && key <= r_hi;
-                            const uint32_t slot = warp_reserve(&s.ctl->ncand, keep, lane);
+                            const uint32_t slot = warp_reserve(CTL(s, ncand), keep, lane);
                             if (keep) {
                                 if (slot < cap) {
-                                    s.cand_key[slot] = key;
-                                    s.cand_idx[slot] = idx;
+                                    ptx::sts_u32(s.cand_key + 4u * slot, key);
+                                    ptx::sts_u32(s.cand_idx + 4u * slot, idx);
                                 } else {
-                                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                    set_err(TOPK_FLAG_INTERNAL);
                                 }
                             }
                         }
@@ -729,10 +738,10 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 // One more 11-bit round over [r_lo, r_hi].
                 const int sh = shift_for_span(r_hi - r_lo);
                 if (!stream_mode) {
-                    const uint32_t nc = s.ctl->ncand;
+                    const uint32_t nc = ptx::lds_u32(CTL(s, ncand));
                     for (uint32_t i = tid; i < nc; i += NT) {
-                        const uint32_t key = s.cand_key[i];
-                        if (key >= r_lo && key <= r_hi) atomicAdd(&h_next[(key - r_lo) >> sh], 1u);
+                        const uint32_t key = ptx::lds_u32(s.cand_key + 4u * i);
+                        if (key >= r_lo && key <= r_hi) ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
                     }
                 } else {
                     for (uint32_t v = tid; v < nvec_slice; v += NT) {
@@ -742,19 +751,20 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         for (int c = 0; c < 4; ++c) {
                             const uint32_t idx = s0 + 4u * v + c;
                             const uint32_t key = score_key(xs[c]);
-                            if (idx < s1 && key >= r_lo && key <= r_hi) atomicAdd(&h_next[(key - r_lo) >> sh], 1u);
+                            if (idx < s1 && key >= r_lo && key <= r_hi)
+                                ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
                         }
                     }
                 }
                 __syncthreads();
-                const uint32_t* hr = h_next;
+                uint32_t hr = h_next;
                 if (C > 1) {
                     cluster_merge<NT, C>(s, h_next, rank, tid);
                     hr = s.hist_m;
                 }
                 sr = scan_find<NT>(s, hr, Kp - G, tid, h_next);
                 if (sr.bin >= static_cast<uint32_t>(kBins)) {  // cannot happen: the bin holds >= need
-                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                    set_err(TOPK_FLAG_INTERNAL);
                     clear_hist<NT>(h_next, tid);
                     break;
                 }
@@ -767,7 +777,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 r_hi = nhi;
                 cnt = sr.count;
                 clear_hist<NT>(h_next, tid);
-                uint32_t* t = h_next;
+                const uint32_t t = h_next;
                 h_next = h_other;
                 h_other = t;
             }
@@ -779,17 +789,16 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 const uint32_t T = r_lo;
                 uint32_t quota = need;
                 if (C > 1) {
-                    if (tid < C) ptx::st_cluster_u32(ptx::map_rank(ptx::smem_addr(&s.ctl->rank_eq[rank]), tid),
-                                                     local_cnt);
+                    if (tid < C) ptx::st_cluster_u32(ptx::map_rank(CTL(s, rank_eq) + 4u * rank, tid), local_cnt);
                     ptx::cluster_sync();
                     uint32_t before = 0;
-                    for (uint32_t q = 0; q < rank; ++q) before += s.ctl->rank_eq[q];
+                    for (uint32_t q = 0; q < rank; ++q) before += ptx::lds_u32(CTL(s, rank_eq) + 4u * q);
                     quota = need > before ? min(need - before, local_cnt) : 0u;
                 }
                 const bool all_eq = (quota == local_cnt);
                 if (!stream_mode) {
-                    const uint32_t nc = s.ctl->ncand;
-                    emit_from_buffer(nc, [&](uint32_t key, uint32_t) { return key > T || (all_eq && key == T); });
+                    const uint32_t nc = ptx::lds_u32(CTL(s, ncand));
+                    emit_from_buffer(nc, [&](uint32_t key) { return key > T || (all_eq && key == T); });
                     if (!all_eq && quota > 0) {
                         // The `quota` smallest positions among this block's copies of T:
                         // rounds on v = ~position (larger v = smaller position).
@@ -798,9 +807,9 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                             if (v_lo == v_hi || v_cnt <= static_cast<uint32_t>(kFinish)) break;
                             const int sh = shift_for_span(v_hi - v_lo);
                             for (uint32_t i = tid; i < nc; i += NT) {
-                                const uint32_t v = ~s.cand_idx[i];
-                                if (s.cand_key[i] == T && v >= v_lo && v <= v_hi)
-                                    atomicAdd(&h_next[(v - v_lo) >> sh], 1u);
+                                const uint32_t v = ~ptx::lds_u32(s.cand_idx + 4u * i);
+                                if (ptx::lds_u32(s.cand_key + 4u * i) == T && v >= v_lo && v <= v_hi)
+                                    ptx::red_add_s(h_next + 4u * ((v - v_lo) >> sh), 1u);
                             }
                             __syncthreads();
                             const ScanResult vs = scan_find<NT>(s, h_next, quota - v_g, tid);
@@ -815,30 +824,30 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                             __syncthreads();
                         }
                         // Above the final range: taken.  Inside it: a warp sort picks the rest.
-                        if (tid == 0) s.ctl->nfin = 0;
+                        if (tid == 0) ptx::sts_u32(CTL(s, nfin), 0);
                         __syncthreads();
                         for (uint32_t i0 = warp * 32u; i0 < nc; i0 += NT) {
                             const uint32_t i = i0 + lane;
-                            const bool eq = i < nc && s.cand_key[i] == T;
-                            const uint32_t pos = eq ? s.cand_idx[i] : 0u;
+                            const bool eq = i < nc && ptx::lds_u32(s.cand_key + 4u * i) == T;
+                            const uint32_t pos = eq ? ptx::lds_u32(s.cand_idx + 4u * i) : 0u;
                             const uint32_t v = ~pos;
                             emit_warp(eq && v > v_hi, pos);
                             const bool fin = eq && v >= v_lo && v <= v_hi;
-                            const uint32_t slot = warp_reserve(&s.ctl->nfin, fin, lane);
+                            const uint32_t slot = warp_reserve(CTL(s, nfin), fin, lane);
                             if (fin) {
                                 if (slot < static_cast<uint32_t>(kFinish)) {
-                                    s.fin_key[slot] = v;
-                                    s.fin_idx[slot] = pos;
+                                    ptx::sts_u32(s.fin_key + 4u * slot, v);
+                                    ptx::sts_u32(s.fin_idx + 4u * slot, pos);
                                 } else {
-                                    atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                    set_err(TOPK_FLAG_INTERNAL);
                                 }
                             }
                         }
                         __syncthreads();
                         if (warp == 0) {
-                            const uint32_t nf = min(s.ctl->nfin, static_cast<uint32_t>(kFinish));
+                            const uint32_t nf = min(ptx::lds_u32(CTL(s, nfin)), static_cast<uint32_t>(kFinish));
                             const uint64_t e = lane < static_cast<int>(nf)
-                                                   ? (static_cast<uint64_t>(s.fin_key[lane]) << 32) | 1ull
+                                                   ? (static_cast<uint64_t>(ptx::lds_u32(s.fin_key + 4u * lane)) << 32) | 1ull
                                                    : 0ull;
                             const uint64_t srt = warp_sort_desc(e, lane);
                             const uint32_t take = quota - v_g;
@@ -872,11 +881,11 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         }
                         const uint32_t n_eq = __popc(eqm);
                         const uint32_t incl = warp_inclusive_sum(n_eq, lane);
-                        if (lane == 31) s.warp_tot[warp] = incl;
+                        if (lane == 31) ptx::sts_u32(s.warp_tot + 4u * warp, incl);
                         __syncthreads();
                         uint32_t pre = 0, tot = 0;
                         for (int w = 0; w < NT / 32; ++w) {
-                            const uint32_t t = s.warp_tot[w];
+                            const uint32_t t = ptx::lds_u32(s.warp_tot + 4u * w);
                             pre += (w < warp) ? t : 0u;
                             tot += t;
                         }
@@ -893,29 +902,27 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 }
             } else {
                 // ---- <= 32 candidates in [r_lo, r_hi]: warp compare-and-swap finish
-                const uint32_t nc = s.ctl->ncand;
-                const uint32_t fin_nfin = ptx::smem_addr(&s.ctl->nfin);
-                const uint32_t fin_key0 = ptx::smem_addr(s.fin_key);
-                const uint32_t fin_idx0 = ptx::smem_addr(s.fin_idx);
-                emit_from_buffer(nc, [&](uint32_t key, uint32_t) { return key > r_hi; });
+                const uint32_t nc = ptx::lds_u32(CTL(s, ncand));
+                emit_from_buffer(nc, [&](uint32_t key) { return key > r_hi; });
                 for (uint32_t i = tid; i < nc; i += NT) {
-                    const uint32_t key = s.cand_key[i];
+                    const uint32_t key = ptx::lds_u32(s.cand_key + 4u * i);
                     if (key >= r_lo && key <= r_hi) {
+                        const uint32_t pos = ptx::lds_u32(s.cand_idx + 4u * i);
                         if (C > 1) {
-                            const uint32_t slot = ptx::atom_add_cluster_u32(ptx::map_rank(fin_nfin, 0), 1u);
+                            const uint32_t slot = ptx::atom_add_cluster_u32(ptx::map_rank(CTL(s, nfin), 0), 1u);
                             if (slot < static_cast<uint32_t>(kFinish)) {
-                                ptx::st_cluster_u32(ptx::map_rank(fin_key0 + slot * 4u, 0), key);
-                                ptx::st_cluster_u32(ptx::map_rank(fin_idx0 + slot * 4u, 0), s.cand_idx[i]);
+                                ptx::st_cluster_u32(ptx::map_rank(s.fin_key + slot * 4u, 0), key);
+                                ptx::st_cluster_u32(ptx::map_rank(s.fin_idx + slot * 4u, 0), pos);
                             } else {
-                                atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                set_err(TOPK_FLAG_INTERNAL);
                             }
                         } else {
-                            const uint32_t slot = atomicAdd(&s.ctl->nfin, 1u);
+                            const uint32_t slot = ptx::atom_add_s(CTL(s, nfin), 1u);
                             if (slot < static_cast<uint32_t>(kFinish)) {
-                                s.fin_key[slot] = key;
-                                s.fin_idx[slot] = s.cand_idx[i];
+                                ptx::sts_u32(s.fin_key + 4u * slot, key);
+                                ptx::sts_u32(s.fin_idx + 4u * slot, pos);
                             } else {
-                                atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                                set_err(TOPK_FLAG_INTERNAL);
                             }
                         }
                     }
@@ -925,10 +932,12 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 else
                     __syncthreads();
                 if (rank == 0 && warp == 0) {
-                    const uint32_t nf = min(s.ctl->nfin, static_cast<uint32_t>(kFinish));
-                    const uint64_t e = lane < static_cast<int>(nf)
-                                           ? (static_cast<uint64_t>(s.fin_key[lane]) << 32) | (~s.fin_idx[lane])
-                                           : 0ull;
+                    const uint32_t nf = min(ptx::lds_u32(CTL(s, nfin)), static_cast<uint32_t>(kFinish));
+                    const uint64_t e =
+                        lane < static_cast<int>(nf)
+                            ? (static_cast<uint64_t>(ptx::lds_u32(s.fin_key + 4u * lane)) << 32) |
+                                  (~ptx::lds_u32(s.fin_idx + 4u * lane))
+                            : 0ull;
                     const uint64_t srt = warp_sort_desc(e, lane);
                     emit_warp(static_cast<uint32_t>(lane) < need && srt != 0ull,
                               ~static_cast<uint32_t>(srt & 0xffffffffull));
@@ -937,29 +946,28 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             __syncthreads();
 
             // ------------------------------------------- 4. transform + write
-            const uint32_t nemit = min(s.ctl->nemit, K);
+            const uint32_t nemit = min(ptx::lds_u32(CTL(s, nemit)), K);
             if (C == 1) {
-                if (nemit != Kp && tid == 0) atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                if (nemit != Kp && tid == 0) set_err(TOPK_FLAG_INTERNAL);
                 for (uint32_t q = tid; q < K; q += NT) {
-                    const int32_t r = q < nemit ? static_cast<int32_t>(s.emit[q]) : -1;
+                    const int32_t r = q < nemit ? static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q)) : -1;
                     out_row[q] = page_map(pt_row, p.log2_page, r);
                     if (raw_row) raw_row[q] = r;
                 }
             } else {
-                if (tid < C)
-                    ptx::st_cluster_u32(ptx::map_rank(ptx::smem_addr(&s.ctl->rank_cnt[rank]), tid), nemit);
+                if (tid < C) ptx::st_cluster_u32(ptx::map_rank(CTL(s, rank_cnt) + 4u * rank, tid), nemit);
                 ptx::cluster_sync();
                 uint32_t before = 0, total = 0;
                 for (uint32_t q = 0; q < static_cast<uint32_t>(C); ++q) {
-                    const uint32_t c = s.ctl->rank_cnt[q];
+                    const uint32_t c = ptx::lds_u32(CTL(s, rank_cnt) + 4u * q);
                     before += (q < rank) ? c : 0u;
                     total += c;
                 }
-                if (rank == 0 && tid == 0 && total != Kp) atomicOr(&s.ctl->err, TOPK_FLAG_INTERNAL);
+                if (rank == 0 && tid == 0 && total != Kp) set_err(TOPK_FLAG_INTERNAL);
                 for (uint32_t q = tid; q < nemit; q += NT) {
                     const uint32_t slot = before + q;
                     if (slot < K) {
-                        const int32_t r = static_cast<int32_t>(s.emit[q]);
+                        const int32_t r = static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q));
                         out_row[slot] = page_map(pt_row, p.log2_page, r);
                         if (raw_row) raw_row[slot] = r;
                     }
@@ -983,7 +991,8 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             if (!ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns)) break;
             ++cseq;
         }
-        if (s.ctl->err) atomicOr(p.flags, s.ctl->err);
+        const uint32_t err = ptx::lds_u32(CTL(s, err));
+        if (err) atomicOr(p.flags, err);
     }
     if (C > 1) ptx::cluster_sync();  // no block leaves while others may still address its shared memory
 }
