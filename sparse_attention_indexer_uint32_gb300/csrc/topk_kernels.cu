@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
     s.ctl_ptr = reinterpret_cast<Control*>(smem_raw + lay.ctl);
 
     constexpr int kSamplesPerThread = kMaxSamples / NT;
-    constexpr int kVecPerStep = 2;  // float4s per thread per reservation step
+    constexpr int kMaxVecPerTile = 8;  // float4s per thread per bulk-copy tile, at most (mask is 32 bits)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = (C > 1) ? ptx::cluster_ctarank() : 0u;
     const uint32_t unit = (C > 1) ? ptx::cluster_id_x() : blockIdx.x;
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
 
     const uint32_t K = static_cast<uint32_t>(p.k);
     const uint32_t cap = static_cast<uint32_t>(p.cap);
-    const uint32_t tile = static_cast<uint32_t>(p.tile);  // a multiple of 4 * kVecPerStep * NT floats
+    const uint32_t tile = static_cast<uint32_t>(p.tile);  // a multiple of 4 * NT floats, <= 4 * 8 * NT
     const uint32_t vec_per_tile = tile / (4u * NT);       // float4s per thread per bulk-copy tile
     const uint32_t stages = static_cast<uint32_t>(p.stages);
 
@@ -570,44 +570,38 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 const uint32_t nvec = min(tile, n4 - off) >> 2;
                 const uint32_t ring_st = s.ring + st * tile * 4u;
                 const uint32_t base_idx = s0 + off;
-                // Each thread takes float4s v = q * NT + tid of the tile, keeps their
-                // keys in registers, counts the gated ones in the histogram and
-                // reserves their buffer slots with one warp-wide reservation per step.
-#pragma unroll 1
-                for (uint32_t q0 = 0; q0 < vec_per_tile; q0 += kVecPerStep) {
-                    uint32_t keys[4 * kVecPerStep];
-                    uint32_t gmask = 0;
+                // Each thread tests float4s v = q * NT + tid of the tile against the
+                // gate into a bitmask (no per-element branches); one warp-wide
+                // reservation per tile; only the gated elements, a small fraction,
+                // are then re-read for the histogram and the candidate buffer.
+                const uint32_t lim = min(s1 - base_idx, tile);  // valid elements in this tile
+                uint32_t gmask = 0;
 #pragma unroll
-                    for (int q = 0; q < kVecPerStep; ++q) {
-                        const uint32_t v = (q0 + q) * NT + tid;
-                        const bool in = v < nvec;
-                        const float4 x = in ? ptx::lds_f4(ring_st + 16u * v) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t key = score_key(xs[c]);
-                            keys[4 * q + c] = key;
-                            const bool gated = in && key >= lo && base_idx + 4u * v + c < s1;
-                            if (gated) {
-                                ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
-                                               1u);
-                                gmask |= 1u << (4 * q + c);
-                            }
-                        }
+                for (int q = 0; q < kMaxVecPerTile; ++q) {
+                    if (q < static_cast<int>(vec_per_tile)) {
+                        const uint32_t v = q * NT + tid;
+                        const float4 x = ptx::lds_f4(ring_st + 16u * v);
+                        const uint32_t e0 = 4u * v;
+                        const uint32_t g = (score_key(x.x) >= lo ? 1u : 0u) | (score_key(x.y) >= lo ? 2u : 0u) |
+                                           (score_key(x.z) >= lo ? 4u : 0u) | (score_key(x.w) >= lo ? 8u : 0u);
+                        const uint32_t valid = e0 + 4u <= lim ? 15u : (e0 >= lim ? 0u : (1u << (lim - e0)) - 1u);
+                        gmask |= (g & valid) << (4 * q);
                     }
+                }
+                uint32_t slot = buffering ? warp_reserve_n(CTL(s, ncand), __popc(gmask), lane) : 0u;
+                while (gmask) {
+                    const int e = __ffs(gmask) - 1;
+                    gmask &= gmask - 1u;
+                    const uint32_t v = static_cast<uint32_t>(e >> 2) * NT + tid;
+                    const uint32_t idx_in_tile = 4u * v + static_cast<uint32_t>(e & 3);
+                    const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
+                    ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)), 1u);
                     if (buffering) {
-                        uint32_t slot = warp_reserve_n(CTL(s, ncand), __popc(gmask), lane);
-#pragma unroll
-                        for (int e = 0; e < 4 * kVecPerStep; ++e) {
-                            if (gmask >> e & 1u) {
-                                if (slot < cap) {
-                                    ptx::sts_u32(s.cand_key + 4u * slot, keys[e]);
-                                    ptx::sts_u32(s.cand_idx + 4u * slot,
-                                                 base_idx + 4u * ((q0 + (e >> 2)) * NT + tid) + (e & 3));
-                                }
-                                ++slot;
-                            }
+                        if (slot < cap) {
+                            ptx::sts_u32(s.cand_key + 4u * slot, key);
+                            ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
                         }
+                        ++slot;
                     }
                 }
                 __syncwarp();
