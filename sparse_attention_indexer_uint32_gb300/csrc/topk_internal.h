@@ -84,12 +84,13 @@ struct __align__(16) Control {
     uint32_t rank_eq[kMaxCluster];   // per-rank copies of the threshold key (tie quotas)
     uint32_t err;
     uint32_t res_local;   // the local (un-merged) count of the bin found by the last scan
-    uint32_t pad[2];
+    uint32_t win_tiles;   // bulk-copy tiles in the current window of work items
+    uint32_t pad[1];
 };
 
 struct Layout {
     uint32_t ring, hist_a, hist_b, hist_m, cand_key, cand_idx, emit, fin_key, fin_idx, warp_tot, ctl;
-    uint32_t items_row, items_len, items_tiles, mbar, total;
+    uint32_t items_row, items_len, items_tiles, items_tile_start, claim, mbar, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -125,6 +126,10 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
     o += kItemsMax * 4u;
     l.items_tiles = o;
     o += kItemsMax * 4u;
+    l.items_tile_start = o;
+    o += kItemsMax * 4u;
+    l.claim = o;
+    o += align_up(static_cast<uint32_t>(stages), 4) * 4u;
     l.mbar = align_up(o, 8);
     o = l.mbar + 2u * stages * 8u;
     l.total = align_up(o, 128);

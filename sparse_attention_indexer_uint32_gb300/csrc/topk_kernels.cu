@@ -124,7 +124,8 @@ struct ScanResult {
 // 32-bit shared-window addresses of the block's shared-memory regions.
 struct Smem {
     uint32_t ring, hist_a, hist_b, hist_m, cand_key, cand_idx, emit, fin_key, fin_idx, warp_tot, ctl;
-    uint32_t it_row, it_len, it_tiles;
+    uint32_t it_row, it_len, it_tiles, it_tile_start, claim;
+    uint32_t* claim_ptr;
     uint64_t* full;
     uint64_t* empty;
     Control* ctl_ptr;
@@ -300,6 +301,9 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
     s.it_row = sbase + lay.items_row;
     s.it_len = sbase + lay.items_len;
     s.it_tiles = sbase + lay.items_tiles;
+    s.it_tile_start = sbase + lay.items_tile_start;
+    s.claim = sbase + lay.claim;
+    s.claim_ptr = reinterpret_cast<uint32_t*>(smem_raw + lay.claim);
     s.full = reinterpret_cast<uint64_t*>(smem_raw + lay.mbar);
     s.empty = s.full + p.stages;
     s.ctl_ptr = reinterpret_cast<Control*>(smem_raw + lay.ctl);
@@ -341,6 +345,7 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
         ptx::sts_u32(CTL(s, nfin), 0);
         ptx::sts_u32(CTL(s, smax), 0);
         ptx::sts_u32(CTL(s, err), 0);
+        for (uint32_t i = 0; i < stages; ++i) ptx::sts_u32(s.claim + 4u * i, 0xffffffffu);
     }
     clear_hist<NT>(s.hist_a, tid);
     clear_hist<NT>(s.hist_b, tid);
@@ -351,11 +356,9 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
     const uint32_t m_max = static_cast<uint32_t>(p.samples);
     auto set_err = [&](uint32_t f) { atomicOr(&s.ctl_ptr->err, f); };
 
-    // Producer state (meaningful in thread 0 only) and the consumer sequence.
-    uint32_t pseq = 0, cseq = 0;
-    int32_t p_item = 0;
-    uint32_t p_tile = 0;
-    bool aborted = false;
+    // Consumer tile sequence number (the same in every thread); tile t of the
+    // sequence lives in ring stage t % stages.
+    uint32_t cseq = 0;
 
     auto slice_of = [&](int32_t L, uint32_t& s0, uint32_t& s1) {
         const uint32_t chunk = ((static_cast<uint32_t>(L) + C - 1) / C + 3u) & ~3u;
@@ -392,49 +395,63 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             ptx::sts_u32(s.it_tiles + 4u * i, nt);
         }
         __syncthreads();
-        p_item = 0;
-        p_tile = 0;
-
-        // Thread 0 keeps the ring full: tiles up to `must` are issued even if
-        // that means waiting for a stage to drain; later ones only if a stage
-        // is already free.
-        auto pump = [&](uint32_t must) {
-            while (p_item < nw && pseq < cseq + stages && !aborted) {
-                const uint32_t nt = ptx::lds_u32(s.it_tiles + 4u * p_item);
-                if (nt == 0) {
-                    ++p_item;
-                    p_tile = 0;
-                    continue;
-                }
-                const uint32_t st = pseq % stages;
-                if (pseq >= stages) {
-                    const uint32_t par = ((pseq / stages) - 1u) & 1u;
-                    if (pseq <= must) {
-                        if (!ptx::mbar_wait_bounded(&s.empty[st], par, p.timeout_ns)) {
-                            aborted = true;
-                            set_err(TOPK_FLAG_TIMEOUT);
-                            break;
-                        }
-                    } else if (!ptx::mbar_test_wait(&s.empty[st], par)) {
-                        break;
-                    }
-                }
-                const int32_t L = static_cast<int32_t>(ptx::lds_u32(s.it_len + 4u * p_item));
-                uint32_t s0, s1;
-                slice_of(L, s0, s1);
-                const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
-                const uint32_t off = p_tile * tile;
-                const uint32_t elems = min(tile, n4 - off);
-                const int32_t prow = static_cast<int32_t>(ptx::lds_u32(s.it_row + 4u * p_item));
-                const float* src = p.scores + static_cast<int64_t>(prow) * p.row_stride + s0 + off;
-                ptx::mbar_arrive_expect_tx(&s.full[st], elems * 4u);
-                ptx::bulk_copy_g2s_addr(s.ring + st * tile * 4u, src, elems * 4u, &s.full[st], policy);
-                ++pseq;
-                if (++p_tile == nt) {
-                    ++p_item;
-                    p_tile = 0;
-                }
+        // Tile sequence of this window: exclusive prefix of the items' tile counts.
+        if (tid == 0) {
+            uint32_t run = 0;
+            for (int32_t i = 0; i < nw; ++i) {
+                ptx::sts_u32(s.it_tile_start + 4u * i, run);
+                run += ptx::lds_u32(s.it_tiles + 4u * i);
             }
+            ptx::sts_u32(CTL(s, win_tiles), run);
+        }
+        __syncthreads();
+        const uint32_t win_base = cseq;
+        const uint32_t win_end = win_base + ptx::lds_u32(CTL(s, win_tiles));
+
+        // Issues the bulk copy of window tile `t` (global sequence number) into
+        // stage t % stages and records its round in the stage's claim word.
+        auto issue_tile = [&](uint32_t t) {
+            const uint32_t qw = t - win_base;
+            int32_t lo_i = 0, hi_i = nw - 1;  // largest item whose first tile is <= qw
+            while (lo_i < hi_i) {
+                const int32_t mid = (lo_i + hi_i + 1) >> 1;
+                if (ptx::lds_u32(s.it_tile_start + 4u * mid) <= qw)
+                    lo_i = mid;
+                else
+                    hi_i = mid - 1;
+            }
+            const uint32_t tile_in_item = qw - ptx::lds_u32(s.it_tile_start + 4u * lo_i);
+            const int32_t L = static_cast<int32_t>(ptx::lds_u32(s.it_len + 4u * lo_i));
+            uint32_t t0, t1;
+            slice_of(L, t0, t1);
+            const uint32_t n4 = ((t1 + 3u) & ~3u) - t0;
+            const uint32_t off = tile_in_item * tile;
+            const uint32_t elems = min(tile, n4 - off);
+            const int32_t prow = static_cast<int32_t>(ptx::lds_u32(s.it_row + 4u * lo_i));
+            const float* src = p.scores + static_cast<int64_t>(prow) * p.row_stride + t0 + off;
+            const uint32_t st = t % stages;
+            ptx::mbar_arrive_expect_tx(&s.full[st], elems * 4u);
+            ptx::bulk_copy_g2s_addr(s.ring + st * tile * 4u, src, elems * 4u, &s.full[st], policy);
+        };
+        // Initial fill: the stages are all free at a window boundary.
+        if (tid == 0) {
+            for (uint32_t t = win_base; t < win_end && t < win_base + stages; ++t) {
+                ptx::sts_u32(s.claim + 4u * (t % stages), t / stages);
+                issue_tile(t);
+            }
+        }
+        // Called by lane 0 of every warp after it released tile t: the warp
+        // whose release completed the stage refills it with tile t + stages
+        // (one claim per stage and round), so the ring is refilled as soon as
+        // the slowest warp is done, not when a designated producer gets to it.
+        auto refill_after = [&](uint32_t t) {
+            const uint32_t next = t + stages;
+            if (next >= win_end) return;
+            const uint32_t st = t % stages;
+            const uint32_t r = t / stages;
+            if (!ptx::mbar_test_wait(&s.empty[st], r & 1u)) return;
+            if (atomicCAS(&s.claim_ptr[st], r, r + 1u) != r) return;
+            issue_tile(next);
         };
 
         // Samples per row: 1024 for rows up to 16K, more for longer rows.
@@ -557,14 +574,10 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             // ------------------------------------------------- 2. pass 1
             const bool buffering = !p.force_two_pass;
             for (uint32_t t = 0; t < ntiles; ++t) {
-                if (tid == 0) pump(cseq);
-                __syncwarp();
                 const uint32_t st = cseq % stages;
                 const bool gave_up = (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) != 0u;
-                if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns)) {
+                if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns))
                     set_err(TOPK_FLAG_TIMEOUT);
-                    aborted = true;
-                }
                 const uint32_t off = t * tile;
                 const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
                 const uint32_t nvec = min(tile, n4 - off) >> 2;
@@ -605,11 +618,13 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                     }
                 }
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&s.empty[st]);
+                if (lane == 0) {
+                    ptx::mbar_arrive(&s.empty[st]);
+                    refill_after(cseq);
+                }
                 ++cseq;
             }
             __syncthreads();
-            if (tid == 0) pump(0);  // prefetch the next row while this one resolves
 
             const uint32_t local_ovf = (!buffering || ptx::lds_u32(CTL(s, ncand)) > cap) ? 1u : 0u;
             uint32_t hm = s.hist_a;
@@ -978,12 +993,12 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
         __syncthreads();
     }
 
-    // Drain: nothing may still be copying into this block's shared memory.
-    if (tid == 0) {
-        while (pseq > cseq) {
-            const uint32_t st = cseq % stages;
-            if (!ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns)) break;
-            ++cseq;
+    // Drain: every issued tile was consumed unless a wait gave up; then the
+    // last copy of each stage is waited for (bounded) before the block exits.
+    if (tid == 0 && (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT)) {
+        for (uint32_t st = 0; st < stages; ++st) {
+            const uint32_t r = ptx::lds_u32(s.claim + 4u * st);
+            if (r != 0xffffffffu) ptx::mbar_wait_bounded(&s.full[st], r & 1u, p.timeout_ns);
         }
         const uint32_t err = ptx::lds_u32(CTL(s, err));
         if (err) atomicOr(p.flags, err);
