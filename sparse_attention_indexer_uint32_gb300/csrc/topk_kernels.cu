@@ -1023,7 +1023,9 @@ __device__ __forceinline__ int length_bucket(int32_t L) {
 // loaded into registers up front (no dependent load chain), and the lanes of
 // a warp that share a (class, bucket) combine their atomics.
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanPerThread = 16;
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kPlanPerThread = 16;  // rows held in registers per thread in one sweep
+constexpr int kPlanKeys = 128;      // 2 classes x 64 length buckets
 
 __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t max_seq_len, uint32_t* flags) {
     if (L < 0) {
@@ -1037,71 +1039,94 @@ __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t max_seq_len, uin
     return L;
 }
 
+// Each row gets the key (class, bucket): long rows (L > threshold) take keys
+// 64..127, short rows 0..63, longer buckets higher.  The lists are written in
+// descending key order, so position = (rows with a higher key) + (rows with
+// the same key counted before it).  Counts are kept per warp (no contention
+// between warps) and turned into per-warp starting offsets by one block-wide
+// exclusive scan over (key descending, warp ascending).
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_lens, int32_t batch,
                                                             int32_t max_seq_len, int32_t threshold, void* ws) {
-    __shared__ uint32_t cnt[128];
-    __shared__ uint32_t cur[128];
-    __shared__ uint32_t total[2];
+    __shared__ uint32_t cnt[kPlanKeys][kPlanWarps];  // per-warp counts, then per-warp cursors
+    __shared__ uint32_t warp_sum[kPlanWarps];
     __shared__ uint32_t flags_s;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int i = tid; i < 128; i += kPlanThreads) cnt[i] = 0;
-    if (tid == 0) flags_s = 0;
-    __syncthreads();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int32_t* lists[2] = {plan_short_list(ws, batch), plan_long_list(ws)};
     uint32_t flags = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int32_t base = 0; base < batch; base += kPlanThreads * kPlanPerThread) {
-            int32_t len[kPlanPerThread];
+    if (tid == 0) flags_s = 0;
+    uint32_t n_long_total = 0;
+    for (int32_t base = 0; base < batch; base += kPlanThreads * kPlanPerThread) {
+        uint32_t* c = &cnt[0][0];
+        for (int i = tid; i < kPlanKeys * kPlanWarps; i += kPlanThreads) c[i] = 0;
+        __syncthreads();
+        uint32_t key[kPlanPerThread];
 #pragma unroll
-            for (int q = 0; q < kPlanPerThread; ++q) {
-                const int32_t b = base + q * kPlanThreads + tid;
-                len[q] = b < batch ? __ldg(seq_lens + b) : 0;
-            }
-#pragma unroll
-            for (int q = 0; q < kPlanPerThread; ++q) {
-                if (base + q * kPlanThreads >= batch) break;  // the same for the whole block
-                const int32_t b = base + q * kPlanThreads + tid;
-                const bool valid = b < batch;
-                const int32_t L = clamp_len(len[q], max_seq_len, &flags);
-                const uint32_t key = valid ? static_cast<uint32_t>((L > threshold ? 64 : 0) + length_bucket(L)) : 255u;
-                const uint32_t peers = __match_any_sync(kFull, key);
-                const int leader = __ffs(peers) - 1;
-                uint32_t pos = 0;
-                if (lane == leader && valid) {
-                    if (pass == 0)
-                        atomicAdd(&cnt[key], __popc(peers));
-                    else
-                        pos = atomicAdd(&cur[key], __popc(peers));
-                }
-                if (pass == 1) {
-                    pos = __shfl_sync(kFull, pos, leader) + __popc(peers & lt_mask);
-                    if (valid) lists[key >> 6][pos] = b;
-                }
+        for (int q = 0; q < kPlanPerThread; ++q) {
+            const int32_t b = base + q * kPlanThreads + tid;
+            key[q] = 0xffffffffu;
+            if (b < batch) {
+                const int32_t L = clamp_len(__ldg(seq_lens + b), max_seq_len, &flags);
+                key[q] = static_cast<uint32_t>((L > threshold ? 64 : 0) + length_bucket(L));
             }
         }
-        if (pass == 0) {
-            if (flags) atomicOr(&flags_s, flags);
-            __syncthreads();
-            if (tid < 2) {  // exclusive offsets within each class, longest bucket first
-                uint32_t run = 0;
-                for (int k = 63; k >= 0; --k) {
-                    cur[tid * 64 + k] = run;
-                    run += cnt[tid * 64 + k];
-                }
-                total[tid] = run;
-            }
-            __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kPlanPerThread; ++q)
+            if (key[q] != 0xffffffffu) atomicAdd(&cnt[key[q]][warp], 1u);
+        __syncthreads();
+        // Exclusive scan over entries e = 0..4095 ordered (key desc, warp asc):
+        // thread t owns entries 4t..4t+3, which share one key.
+        const uint32_t k = kPlanKeys - 1 - (4 * tid) / kPlanWarps;
+        const int w0 = (4 * tid) % kPlanWarps;
+        uint32_t v[4], sum = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            v[u] = cnt[k][w0 + u];
+            sum += v[u];
         }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        uint32_t pre = 0, n_long = 0;
+        for (int w = 0; w < kPlanWarps; ++w) {
+            const uint32_t t = warp_sum[w];
+            pre += (w < warp) ? t : 0u;
+            n_long += (w < kPlanWarps / 2) ? t : 0u;  // keys 64..127 are the first half of the order
+        }
+        uint32_t run = pre + incl - sum;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            cnt[k][w0 + u] = run;
+            run += v[u];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kPlanPerThread; ++q) {
+            if (key[q] == 0xffffffffu) continue;
+            const uint32_t pos = atomicAdd(&cnt[key[q]][warp], 1u);
+            const int32_t b = base + q * kPlanThreads + tid;
+            if (key[q] >= 64u)
+                lists[1][n_long_total + pos] = b;
+            else
+                lists[0][(static_cast<uint32_t>(base) - n_long_total) + (pos - n_long)] = b;
+        }
+        n_long_total += n_long;
+        __syncthreads();
     }
+    if (flags) atomicOr(&flags_s, flags);
+    __syncthreads();
     if (tid == 0) {
         PlanHeader* h = static_cast<PlanHeader*>(ws);
         h->magic = kPlanMagic;
         h->batch = batch;
         h->max_seq_len = max_seq_len;
         h->long_threshold = threshold;
-        h->n_long = static_cast<int32_t>(total[1]);
-        h->n_short = static_cast<int32_t>(total[0]);
+        h->n_long = static_cast<int32_t>(n_long_total);
+        h->n_short = batch - static_cast<int32_t>(n_long_total);
         h->flags = flags_s;
     }
 }
