@@ -152,7 +152,8 @@ def config_of(wl: workloads.Workload, name: str, world: int) -> dict:
     return {"workload": wl.name, "kind": name, "batch": wl.batch, "seq_len": int(eff.max()),
             "sum_seq_len": int(eff.sum()), "k": wl.k, "page_size": wl.page_size, "row_stride": wl.row_stride,
             "raw_output": wl.want_raw, "global_batch": wl.batch * world, "parallelism": f"replica{world}",
-            "l2": "flushed between timed steps (256 MB write); inputs > L2 for decode/throughput"}
+            "l2": "flushed between timed steps (256 MB write); inputs > L2 for decode/throughput",
+            "launch": "plan and transform replayed from CUDA graphs; events on the launching stream"}
 
 
 def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: bool):
@@ -184,6 +185,20 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     n_long_launch = 1 if wl.max_seq_len > _threshold(wl.batch) else 0
     launches_per_step = 2 + n_long_launch  # plan + short-row select (+ long-row cluster select)
 
+    # Each step's two calls are replayed from CUDA graphs, so host launch
+    # latency does not leak into the timed region between the events.
+    g_plan, g_sel = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plan):
+        _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws)
+    with torch.cuda.graph(g_sel):
+        _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
+                            wl.page_size, wl.k, out, raw, ws)
+    for _ in range(2):
+        flush.fill_(1.0)
+        g_plan.replay()
+        g_sel.replay()
+    torch.cuda.synchronize(dev)
+
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if world > 1:
@@ -196,10 +211,9 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     for e0, e1, e2 in ev:
         flush.fill_(1.0)
         e0.record(stream)
-        _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws, stream)
+        g_plan.replay()
         e1.record(stream)
-        _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
-                            wl.page_size, wl.k, out, raw, ws, stream)
+        g_sel.replay()
         e2.record(stream)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall

@@ -570,6 +570,10 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 }
             }
             load_samples(j + 1);
+            // The float at the bottom of the gate: key(x) >= lo <=> !(x < f_lo) for
+            // every non-NaN x (the inverse of the key map; lo = 0 gives a NaN,
+            // so that everything passes).
+            const float f_lo = __uint_as_float((lo & 0x80000000u) ? (lo & 0x7fffffffu) : ~lo);
 
             // ------------------------------------------------- 2. pass 1
             const bool buffering = !p.force_two_pass;
@@ -584,21 +588,38 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 const uint32_t ring_st = s.ring + st * tile * 4u;
                 const uint32_t base_idx = s0 + off;
                 // Each thread tests float4s v = q * NT + tid of the tile against the
-                // gate into a bitmask (no per-element branches); one warp-wide
-                // reservation per tile; only the gated elements, a small fraction,
-                // are then re-read for the histogram and the candidate buffer.
+                // gate into a bitmask with one float compare per element: with f_lo
+                // the float whose key is lo, !(x < f_lo) holds for every x with
+                // key(x) >= lo, and also for NaNs (and everything, if f_lo is a NaN).
+                // One warp-wide reservation per tile; only the gated elements, a
+                // small fraction, are re-read, keyed exactly, counted in the
+                // histogram and buffered.  A false positive (a NaN under the gate)
+                // fills its reserved slot with key 0, which no later step selects.
                 const uint32_t lim = min(s1 - base_idx, tile);  // valid elements in this tile
                 uint32_t gmask = 0;
+                if (lim == tile) {
 #pragma unroll
-                for (int q = 0; q < kMaxVecPerTile; ++q) {
-                    if (q < static_cast<int>(vec_per_tile)) {
-                        const uint32_t v = q * NT + tid;
-                        const float4 x = ptx::lds_f4(ring_st + 16u * v);
-                        const uint32_t e0 = 4u * v;
-                        const uint32_t g = (score_key(x.x) >= lo ? 1u : 0u) | (score_key(x.y) >= lo ? 2u : 0u) |
-                                           (score_key(x.z) >= lo ? 4u : 0u) | (score_key(x.w) >= lo ? 8u : 0u);
-                        const uint32_t valid = e0 + 4u <= lim ? 15u : (e0 >= lim ? 0u : (1u << (lim - e0)) - 1u);
-                        gmask |= (g & valid) << (4 * q);
+                    for (int q = 0; q < kMaxVecPerTile; ++q) {
+                        if (q < static_cast<int>(vec_per_tile)) {
+                            const float4 x = ptx::lds_f4(ring_st + 16u * (q * NT + tid));
+                            gmask |= ((x.x < f_lo ? 0u : 1u) | (x.y < f_lo ? 0u : 2u) | (x.z < f_lo ? 0u : 4u) |
+                                      (x.w < f_lo ? 0u : 8u))
+                                     << (4 * q);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kMaxVecPerTile; ++q) {
+                        if (q < static_cast<int>(vec_per_tile)) {
+                            const uint32_t v = q * NT + tid;
+                            const float4 x = ptx::lds_f4(ring_st + 16u * v);
+                            const uint32_t e0 = 4u * v;
+                            const uint32_t g = (x.x < f_lo ? 0u : 1u) | (x.y < f_lo ? 0u : 2u) |
+                                               (x.z < f_lo ? 0u : 4u) | (x.w < f_lo ? 0u : 8u);
+                            const uint32_t valid =
+                                e0 + 4u <= lim ? 15u : (e0 >= lim ? 0u : (1u << (lim - e0)) - 1u);
+                            gmask |= (g & valid) << (4 * q);
+                        }
                     }
                 }
                 uint32_t slot = buffering ? warp_reserve_n(CTL(s, ncand), __popc(gmask), lane) : 0u;
@@ -608,10 +629,13 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                     const uint32_t v = static_cast<uint32_t>(e >> 2) * NT + tid;
                     const uint32_t idx_in_tile = 4u * v + static_cast<uint32_t>(e & 3);
                     const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
-                    ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)), 1u);
+                    const bool pass = key >= lo;
+                    if (pass)
+                        ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
+                                       1u);
                     if (buffering) {
                         if (slot < cap) {
-                            ptx::sts_u32(s.cand_key + 4u * slot, key);
+                            ptx::sts_u32(s.cand_key + 4u * slot, pass ? key : 0u);
                             ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
                         }
                         ++slot;
