@@ -1093,9 +1093,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
                 key[q] = static_cast<uint32_t>((L > threshold ? 64 : 0) + length_bucket(L));
             }
         }
+        // Runs of equal keys within a thread's rows take one atomic each (rows
+        // of a batch often share a length, and so every lane of a warp would
+        // otherwise hit the same counter for every row).
+        {
+            uint32_t run_key = key[0], run_len = 0;
 #pragma unroll
-        for (int q = 0; q < kPlanPerThread; ++q)
-            if (key[q] != 0xffffffffu) atomicAdd(&cnt[key[q]][warp], 1u);
+            for (int q = 0; q < kPlanPerThread; ++q) {
+                if (key[q] != run_key) {
+                    if (run_key != 0xffffffffu && run_len) atomicAdd(&cnt[run_key][warp], run_len);
+                    run_key = key[q];
+                    run_len = 0;
+                }
+                ++run_len;
+            }
+            if (run_key != 0xffffffffu && run_len) atomicAdd(&cnt[run_key][warp], run_len);
+        }
         __syncthreads();
         // Exclusive scan over entries e = 0..4095 ordered (key desc, warp asc):
         // thread t owns entries 4t..4t+3, which share one key.
@@ -1128,15 +1141,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
             run += v[u];
         }
         __syncthreads();
+        {
+            // Same runs: one atomic reserves a run's positions (run lengths are
+            // counted backwards first).
+            uint32_t rl[kPlanPerThread];
 #pragma unroll
-        for (int q = 0; q < kPlanPerThread; ++q) {
-            if (key[q] == 0xffffffffu) continue;
-            const uint32_t pos = atomicAdd(&cnt[key[q]][warp], 1u);
-            const int32_t b = base + q * kPlanThreads + tid;
-            if (key[q] >= 64u)
-                lists[1][n_long_total + pos] = b;
-            else
-                lists[0][(static_cast<uint32_t>(base) - n_long_total) + (pos - n_long)] = b;
+            for (int q = kPlanPerThread - 1; q >= 0; --q)
+                rl[q] = (q + 1 < kPlanPerThread && key[q + 1] == key[q]) ? rl[q + 1] + 1u : 1u;
+            uint32_t pos = 0;
+#pragma unroll
+            for (int q = 0; q < kPlanPerThread; ++q) {
+                if (key[q] == 0xffffffffu) continue;
+                if (q == 0 || key[q] != key[q - 1]) pos = atomicAdd(&cnt[key[q]][warp], rl[q]);
+                const int32_t b = base + q * kPlanThreads + tid;
+                if (key[q] >= 64u)
+                    lists[1][n_long_total + pos] = b;
+                else
+                    lists[0][(static_cast<uint32_t>(base) - n_long_total) + (pos - n_long)] = b;
+                ++pos;
+            }
         }
         n_long_total += n_long;
         __syncthreads();
