@@ -622,23 +622,46 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         }
                     }
                 }
-                uint32_t slot = buffering ? warp_reserve_n(CTL(s, ncand), __popc(gmask), lane) : 0u;
-                while (gmask) {
-                    const int e = __ffs(gmask) - 1;
-                    gmask &= gmask - 1u;
-                    const uint32_t v = static_cast<uint32_t>(e >> 2) * NT + tid;
-                    const uint32_t idx_in_tile = 4u * v + static_cast<uint32_t>(e & 3);
-                    const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
-                    const bool pass = key >= lo;
-                    if (pass)
-                        ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
-                                       1u);
-                    if (buffering) {
-                        if (slot < cap) {
-                            ptx::sts_u32(s.cand_key + 4u * slot, pass ? key : 0u);
-                            ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
-                        }
+                // Gated elements: each lane writes only the positions of its gated
+                // elements into its reserved slots; the warp then takes the
+                // compacted slots one per lane to key them exactly, count them in
+                // the histogram and fill in their keys.  When the buffer is full (or
+                // not used) each lane counts its own elements instead.
+                const uint32_t cnt = __popc(gmask);
+                const uint32_t incl = warp_inclusive_sum(cnt, lane);
+                const uint32_t total = __shfl_sync(kFull, incl, 31);
+                uint32_t wbase = 0;
+                if (buffering && lane == 31 && total != 0u) wbase = ptx::atom_add_s(CTL(s, ncand), total);
+                wbase = __shfl_sync(kFull, wbase, 31);
+                if (buffering && wbase + total <= cap) {
+                    uint32_t slot = wbase + incl - cnt;
+                    while (gmask) {
+                        const int e = __ffs(gmask) - 1;
+                        gmask &= gmask - 1u;
+                        const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
+                        ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
                         ++slot;
+                    }
+                    __syncwarp();
+                    for (uint32_t i = lane; i < total; i += 32) {
+                        const uint32_t sl = wbase + i;
+                        const uint32_t idx_in_tile = ptx::lds_u32(s.cand_idx + 4u * sl) - base_idx;
+                        const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
+                        const bool pass = key >= lo;
+                        if (pass)
+                            ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
+                                           1u);
+                        ptx::sts_u32(s.cand_key + 4u * sl, pass ? key : 0u);
+                    }
+                } else {
+                    while (gmask) {
+                        const int e = __ffs(gmask) - 1;
+                        gmask &= gmask - 1u;
+                        const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
+                        const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
+                        if (key >= lo)
+                            ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
+                                           1u);
                     }
                 }
                 __syncwarp();

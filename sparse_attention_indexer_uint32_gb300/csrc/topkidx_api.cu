@@ -88,11 +88,13 @@ int sm_count() {
 // entries (>= 2048), 3 blocks per SM at k = 512.  Clusters: 3 x 16 KB (two
 // blocks per SM) when the long rows can fill the GPU, 5 x 32 KB when they
 // cannot.
-PathConfig path_config(int cluster, int32_t k, int32_t batch, const topk_tuning_t& t) {
+PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_len, const topk_tuning_t& t) {
     PathConfig c;
     c.cluster = cluster;
     const bool few_rows = cluster > 1 && static_cast<int64_t>(batch) * cluster * 2 <= sm_count();
-    c.tile = few_rows ? 8192 : 4096;  // floats per bulk copy: 32 KB or 16 KB
+    // floats per bulk copy: 32 KB for long single-block rows and for few long
+    // cluster rows, 16 KB otherwise (short rows keep 3 blocks per SM).
+    c.tile = (few_rows || (cluster == 1 && max_seq_len > 16384)) ? 8192 : 4096;
     c.stages = cluster == 1 ? 2 : (few_rows ? 5 : 3);
     int cap = t.candidate_capacity;
     if (cap == 0) {
@@ -239,7 +241,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
 
     const bool launch_long = max_seq_len > threshold;
     if (launch_long) {
-        const PathConfig c = path_config(t.cluster_size, k, batch, t);
+        const PathConfig c = path_config(t.cluster_size, k, batch, max_seq_len, t);
         int units = 0;
         const topk_status_t r = resident_units(c.cluster, c.smem, &units);
         if (r != TOPK_OK) return r;
@@ -255,7 +257,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
     }
     {
-        const PathConfig c = path_config(1, k, batch, t);
+        const PathConfig c = path_config(1, k, batch, max_seq_len, t);
         int units = 0;
         const topk_status_t r = resident_units(1, c.smem, &units);
         if (r != TOPK_OK) return r;
