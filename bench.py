@@ -185,8 +185,15 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     n_long_launch = 1 if wl.max_seq_len > _threshold(wl.batch) else 0
     launches_per_step = 2 + n_long_launch  # plan + short-row select (+ long-row cluster select)
 
-    # Each step's two calls are replayed from CUDA graphs, so host launch
-    # latency does not leak into the timed region between the events.
+    # A step (plan + transform) is replayed from one CUDA graph, as a serving
+    # loop would run it: host launch latency stays out of the timed region and
+    # the transform's programmatic launch overlaps the plan's tail.
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws)
+        _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
+                            wl.page_size, wl.k, out, raw, ws)
+    # The same two calls as two graphs, to time the select kernel(s) alone.
     g_plan, g_sel = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_plan):
         _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws)
@@ -195,12 +202,15 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
                             wl.page_size, wl.k, out, raw, ws)
     for _ in range(2):
         flush.fill_(1.0)
+        g_step.replay()
+        flush.fill_(1.0)
         g_plan.replay()
         g_sel.replay()
     torch.cuda.synchronize(dev)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev3 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -208,7 +218,17 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     if sampler:
         sampler.__enter__()
     t_wall = time.perf_counter()
-    for e0, e1, e2 in ev:
+    for e0, e1 in ev:
+        flush.fill_(1.0)
+        e0.record(stream)
+        g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    # Split timing (after the timed region): the plan, then the select kernel(s).
+    for e0, e1, e2 in ev3:
         flush.fill_(1.0)
         e0.record(stream)
         g_plan.replay()
@@ -216,14 +236,11 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         g_sel.replay()
         e2.record(stream)
     torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall
-    if world > 1:
-        dist.barrier()
     if sampler:
         sampler.__exit__(None, None, None)
-    step_ms = [e0.elapsed_time(e2) for e0, _, e2 in ev]
-    plan_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
-    sel_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    plan_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev3]
+    sel_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev3]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)

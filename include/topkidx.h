@@ -222,6 +222,9 @@ typedef struct {
                                            a multiple of 64                                      */
     int32_t samples;                    /* 0: automatic; else at most this many gate samples per
                                            row, 32..2048, a multiple of 32                       */
+    int32_t gate_fill_percent;          /* 0: automatic; else 1..100: the gate is loosened until it
+                                           is expected to pass this share of the candidate buffer
+                                           (never tighter than the sampling bound needs)         */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

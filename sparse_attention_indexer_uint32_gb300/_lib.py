@@ -62,6 +62,7 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("disable_gate", ctypes.c_int32),
         ("candidate_capacity", ctypes.c_int32),
         ("samples", ctypes.c_int32),
+        ("gate_fill_percent", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

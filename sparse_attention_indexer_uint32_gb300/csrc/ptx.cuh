@@ -17,6 +17,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before
+// the previous grid in its stream has finished.  grid_dependency_wait blocks
+// until that grid has completed and its memory writes are visible (it returns
+// at once when the launch was an ordinary one); launch_dependents lets the
+// next grid in the stream start early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------- shared-memory accessors
 // Explicit .shared accesses on 32-bit shared-window addresses, so that hot
 // loops never fall back to generic loads, stores or atomics.  All carry a

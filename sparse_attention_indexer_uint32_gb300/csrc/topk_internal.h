@@ -69,6 +69,7 @@ struct SelectParams {
     int32_t stages;           // bulk-copy ring depth
     int32_t cap;              // candidate buffer entries per block
     int32_t samples;          // gate samples per row
+    float gate_fill;          // share of the candidate buffer the gate aims to fill
     int32_t force_two_pass;
     int32_t disable_gate;
     uint64_t timeout_ns;

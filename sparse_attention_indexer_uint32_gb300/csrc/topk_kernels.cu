@@ -258,7 +258,7 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
 //  1. Gate.  Up to `samples` scores of the row are read (prefetched while the
 //     previous row is processed).  Their keys give a lower bound `lo`: the
 //     sample's r-th largest key, r = max(E + 4 sqrt(E) + 4, the rank that
-//     fills half the candidate buffer), E the expected number of samples in
+//     fills a set share of the candidate buffer), E the expected number of samples in
 //     the top k.  The bin width is chosen so that the sampled range covers
 //     about 1024 of the 2048 bins (the "linear mapping" of the DistRadixTopK
 //     README: bins spread over the range where the threshold lies, so few
@@ -314,26 +314,11 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
     const uint32_t rank = (C > 1) ? ptx::cluster_ctarank() : 0u;
     const uint32_t unit = (C > 1) ? ptx::cluster_id_x() : blockIdx.x;
     const uint32_t nunits = (C > 1) ? ptx::cluster_count_x() : gridDim.x;
-    if (p.plan && (p.plan->magic != kPlanMagic || p.plan->batch != p.batch ||
-                   p.plan->max_seq_len != p.max_seq_len)) {
-        if (tid == 0 && rank == 0 && unit == 0) atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
-        return;  // same for every block of a cluster
-    }
-    const int32_t n_first = min(p.n_items_dev ? *p.n_items_dev : p.n_items_host, p.batch);
-    const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
-    const int32_t n_items = n_first + max(n_second, 0);
-    const int32_t my_items = n_items > static_cast<int32_t>(unit)
-                                 ? (n_items - 1 - static_cast<int32_t>(unit)) / static_cast<int32_t>(nunits) + 1
-                                 : 0;
-    if (my_items <= 0) return;  // same for every block of a cluster
-
-    const uint32_t K = static_cast<uint32_t>(p.k);
-    const uint32_t cap = static_cast<uint32_t>(p.cap);
-    const uint32_t tile = static_cast<uint32_t>(p.tile);  // a multiple of 4 * NT floats, <= 4 * 8 * NT
-    const uint32_t vec_per_tile = tile / (4u * NT);       // float4s per thread per bulk-copy tile
     const uint32_t stages = static_cast<uint32_t>(p.stages);
 
     // ---------------------------------------------------------------- init
+    // Shared memory only: with a programmatic launch this overlaps the tail
+    // of the kernel before (the plan), whose results are read after the wait.
     if (tid == 0) {
         for (uint32_t i = 0; i < stages; ++i) {
             ptx::mbar_init(&s.full[i], 1);
@@ -351,6 +336,27 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
     clear_hist<NT>(s.hist_b, tid);
     __syncthreads();
     if (C > 1) ptx::cluster_sync();  // every block of the cluster is running before any DSMEM access
+    // Every global access of this kernel comes after this point: the
+    // preceding grid in the stream has completed and its writes are visible.
+    ptx::grid_dependency_wait();
+
+    if (p.plan && (p.plan->magic != kPlanMagic || p.plan->batch != p.batch ||
+                   p.plan->max_seq_len != p.max_seq_len)) {
+        if (tid == 0 && rank == 0 && unit == 0) atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
+        return;  // same for every block of a cluster
+    }
+    const int32_t n_first = min(p.n_items_dev ? *p.n_items_dev : p.n_items_host, p.batch);
+    const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
+    const int32_t n_items = n_first + max(n_second, 0);
+    const int32_t my_items = n_items > static_cast<int32_t>(unit)
+                                 ? (n_items - 1 - static_cast<int32_t>(unit)) / static_cast<int32_t>(nunits) + 1
+                                 : 0;
+    if (my_items <= 0) return;  // same for every block of a cluster
+
+    const uint32_t K = static_cast<uint32_t>(p.k);
+    const uint32_t cap = static_cast<uint32_t>(p.cap);
+    const uint32_t tile = static_cast<uint32_t>(p.tile);  // a multiple of 4 * NT floats, <= 4 * 8 * NT
+    const uint32_t vec_per_tile = tile / (4u * NT);       // float4s per thread per bulk-copy tile
 
     const uint64_t policy = ptx::l2_policy_evict_first();
     const uint32_t m_max = static_cast<uint32_t>(p.samples);
@@ -523,12 +529,12 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                 // r = the sample rank used as the gate.  E samples are expected in the
                 // row's top k; r = E + 4 sqrt(E) + 4 keeps the chance that fewer than k
                 // elements pass the gate small (that case is detected and recounted),
-                // and r is raised to aim at half of the on-chip candidate capacity,
-                // since a tighter gate buys nothing once the candidates fit.
+                // and r is raised to aim at a share (p.gate_fill) of the on-chip
+                // candidate capacity, which lowers the chance of a recount further.
                 const uint32_t M = samples_for(static_cast<uint32_t>(L));
                 const float E = static_cast<float>(M) * static_cast<float>(Kp) / static_cast<float>(L);
                 const float r_safe = ceilf(E + 4.0f * sqrtf(E) + 4.0f);
-                const float r_fill = floorf(0.5f * static_cast<float>(cap) * C * static_cast<float>(M) /
+                const float r_fill = floorf(p.gate_fill * static_cast<float>(cap) * C * static_cast<float>(M) /
                                             static_cast<float>(L));
                 const float r_f = fmaxf(r_safe, r_fill);
                 if (!p.disable_gate && r_f < static_cast<float>(M)) {
@@ -764,25 +770,34 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                     __syncthreads();
                     if (tid == 0) ptx::sts_u32(CTL(s, ncand), 0);
                     __syncthreads();
-                    for (uint32_t v0 = warp * 32u; v0 < nvec_slice; v0 += NT) {
-                        const uint32_t v = v0 + lane;
-                        const bool in = v < nvec_slice;
-                        const float4 x = in ? __ldg(slice4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        const float xs[4] = {x.x, x.y, x.z, x.w};
+                    // Four vectors in flight per lane: these re-reads are latency-bound.
+                    for (uint32_t v0 = warp * 32u; v0 < nvec_slice; v0 += 4u * NT) {
+                        float4 xv[4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t idx = s0 + 4u * v + c;
-                            const uint32_t key = score_key(xs[c]);
-                            const bool live = in && idx < s1;
-                            emit_warp(live && key > r_hi, idx);
-                            const bool keep = live && key >= r_lo && key <= r_hi;
-                            const uint32_t slot = warp_reserve(CTL(s, ncand), keep, lane);
-                            if (keep) {
-                                if (slot < cap) {
-                                    ptx::sts_u32(s.cand_key + 4u * slot, key);
-                                    ptx::sts_u32(s.cand_idx + 4u * slot, idx);
-                                } else {
-                                    set_err(TOPK_FLAG_INTERNAL);
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t v = v0 + u * NT + lane;
+                            xv[u] = v < nvec_slice ? __ldg(slice4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t v = v0 + u * NT + lane;
+                            const bool in = v < nvec_slice;
+                            const float xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t idx = s0 + 4u * v + c;
+                                const uint32_t key = score_key(xs[c]);
+                                const bool live = in && idx < s1;
+                                emit_warp(live && key > r_hi, idx);
+                                const bool keep = live && key >= r_lo && key <= r_hi;
+                                const uint32_t slot = warp_reserve(CTL(s, ncand), keep, lane);
+                                if (keep) {
+                                    if (slot < cap) {
+                                        ptx::sts_u32(s.cand_key + 4u * slot, key);
+                                        ptx::sts_u32(s.cand_idx + 4u * slot, idx);
+                                    } else {
+                                        set_err(TOPK_FLAG_INTERNAL);
+                                    }
                                 }
                             }
                         }
@@ -800,15 +815,24 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                         if (key >= r_lo && key <= r_hi) ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
                     }
                 } else {
-                    for (uint32_t v = tid; v < nvec_slice; v += NT) {
-                        const float4 x = __ldg(slice4 + v);
-                        const float xs[4] = {x.x, x.y, x.z, x.w};
+                    for (uint32_t v0 = tid; v0 < nvec_slice; v0 += 4u * NT) {
+                        float4 xv[4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t idx = s0 + 4u * v + c;
-                            const uint32_t key = score_key(xs[c]);
-                            if (idx < s1 && key >= r_lo && key <= r_hi)
-                                ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t v = v0 + u * NT;
+                            xv[u] = v < nvec_slice ? __ldg(slice4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t v = v0 + u * NT;
+                            const float xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t idx = s0 + 4u * v + c;
+                                const uint32_t key = score_key(xs[c]);
+                                if (v < nvec_slice && idx < s1 && key >= r_lo && key <= r_hi)
+                                    ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
+                            }
                         }
                     }
                 }
@@ -1067,8 +1091,8 @@ __device__ __forceinline__ int length_bucket(int32_t L) {
 // classified long (clamped seq_len > threshold) or short, and each class is
 // written as a list ordered by half-octave length bucket, longest first, so
 // that the persistent kernels hand out the longest rows first.  Lengths are
-// loaded into registers up front (no dependent load chain), and the lanes of
-// a warp that share a (class, bucket) combine their atomics.
+// loaded into registers up front (no dependent load chain), and a thread's
+// run of rows with one (class, bucket) takes one atomic.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kPlanPerThread = 16;  // rows held in registers per thread in one sweep
@@ -1098,6 +1122,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
     __shared__ uint32_t warp_sum[kPlanWarps];
     __shared__ uint32_t flags_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // The select kernel that follows waits for this grid's completion before
+    // reading the lists, so it may be placed on the GPU right away.
+    ptx::launch_dependents();
     int32_t* lists[2] = {plan_short_list(ws, batch), plan_long_list(ws)};
     uint32_t flags = 0;
     if (tid == 0) flags_s = 0;
@@ -1250,14 +1277,20 @@ cudaError_t launch_select_t(const SelectParams& p, int grid_units, size_t smem, 
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    // Programmatic serialization: the blocks are placed and initialise their
+    // shared memory while the previous kernel (the plan) finishes; the kernel
+    // waits for it before its first global access.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (C > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = C;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, select_kernel<NT, C>, p);
 }

@@ -35,7 +35,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: 8, the cluster size both the PR and the
 // DistRadixTopK README use.
-topk_tuning_t g_tuning = {32768, 65536, 15, 8, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 8, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -72,6 +72,7 @@ struct PathConfig {
     int stages;
     int cap;
     int samples;
+    float gate_fill;
     size_t smem;
 };
 
@@ -85,7 +86,8 @@ int sm_count() {
 // Launch shape of the select kernel.  Bulk copies are 16 KB (32 KB when few
 // cluster rows must each pull more bytes per SM): smaller copies cost more
 // per byte.  Single blocks: a 2-stage ring and a candidate buffer of 4k
-// entries (>= 2048), 3 blocks per SM at k = 512.  Clusters: 3 x 16 KB (two
+// entries (>= 2048; >= 3072 for rows over 16K), 3 blocks per SM at k = 512
+// on rows up to 16K, 2 on longer rows.  Clusters: 3 x 16 KB (two
 // blocks per SM) when the long rows can fill the GPU, 5 x 32 KB when they
 // cannot.
 PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_len, const topk_tuning_t& t) {
@@ -100,10 +102,16 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
     if (cap == 0) {
         cap = cluster == 1 ? 4 * k : k;
         if (cap < 2048) cap = 2048;
+        // Long single-block rows: the gate count of a row spreads by about
+        // 1/sqrt(rank) around its aim, and a row past the buffer re-reads its
+        // scores; 3072 entries hold the high draws while two blocks still fit
+        // on an SM at k = 512.
+        if (cluster == 1 && max_seq_len > 16384 && cap < 3072) cap = 3072;
         if (cap > 16384) cap = 16384;
         cap = (cap + 63) / 64 * 64;
     }
     c.cap = cap;
+    c.gate_fill = t.gate_fill_percent > 0 ? 0.01f * static_cast<float>(t.gate_fill_percent) : 0.4f;
     int samples = t.samples;
     if (samples == 0 || samples > kMaxSamples) samples = kMaxSamples;
     c.samples = samples;
@@ -176,6 +184,7 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
         return TOPK_EINVAL;
     if (t->samples != 0 && (t->samples < 32 || t->samples > kMaxSamples || t->samples % 32 != 0))
         return TOPK_EINVAL;
+    if (t->gate_fill_percent < 0 || t->gate_fill_percent > 100) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -252,6 +261,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         q.stages = c.stages;
         q.cap = c.cap;
         q.samples = c.samples;
+        q.gate_fill = c.gate_fill;
         const int grid = batch < units ? batch : units;
         const cudaError_t e = launch_select(q, c.cluster, grid, c.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
@@ -272,6 +282,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         q.stages = c.stages;
         q.cap = c.cap;
         q.samples = c.samples;
+        q.gate_fill = c.gate_fill;
         // Equal shares: the fewest blocks that still give every block the
         // same number of rows when all rows are short.
         const int per_unit = (batch + units - 1) / units;

@@ -117,6 +117,20 @@ def test_few_samples_gate_misses(samples):
     compare(wl, out, raw)
 
 
+@pytest.mark.parametrize("fill", [1, 100])
+@pytest.mark.parametrize("cluster", [1, 8])
+def test_gate_fill_extremes(fill, cluster):
+    """fill = 1: the gate sits at its sampling bound, so some rows pass fewer
+    than k elements and are recounted; fill = 100: the gate aims at the whole
+    candidate buffer, so many rows overflow it and re-read their scores."""
+    wl = workloads.random_case(seed=450 + fill + cluster, batch=24, min_len=3000, max_len=200000, k=512,
+                               page_size=64, dist="bf16")
+    thr = 0 if cluster > 1 else 1 << 30
+    with tuning(gate_fill_percent=fill, long_threshold=thr, long_threshold_small_batch=thr):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
 def test_trend_rows_cluster():
     """Rows with a positional trend (the gate's sample must not alias)."""
     wl = workloads.long_context(batch=2, seq_len=300000)
