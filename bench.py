@@ -41,6 +41,13 @@ from sparse_attention_indexer_uint32_gb300 import workloads  # noqa: E402
 METRIC = "top-k+page-transform HBM GB/s (fraction of peak); µs/call at batch 1, seq 1M"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+# The pages' own figures for a workload of the same shape (another machine:
+# context for vs_baseline, not a target), in GB/s.
+PAGES_GBS = {
+    "throughput": (3250.0, "SGLang PR #26788, streaming bandwidth ~3.2-3.3 TB/s at bs >= 2048, seq 65536, "
+                           "k=512 (B200); midpoint"),
+    "decode": (1563.0, "SGLang PR #26788, decode bucket 1563 GB/s at b=8192, s=8192, k=512 (B200)"),
+}
 
 
 def log(*a):
@@ -89,30 +96,77 @@ def profiled_traffic(workload_name: str):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    """Samples the SM clock and the clock-event (throttle) reasons during the
+    timed region: through NVML every millisecond when libnvidia-ml can be
+    loaded (reads only), else through nvidia-smi every 200 ms."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    # NVML clocks-event reason bits (nvml.h) reported by name
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []
+        self.sm = []
+        self.sm_max = []
+        self.reasons = set()
+        self.source = None
         self._stop = threading.Event()
         self._thread = None
+        self._nvml = None
+        self._dev = None
+        try:
+            import ctypes
+
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() == 0:
+                dev = ctypes.c_void_p()
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(dev)) == 0:
+                    self._nvml, self._dev = lib, dev
+        except Exception:
+            self._nvml = None
+
+    def _nvml_sample(self):
+        import ctypes
+
+        mhz, mx, r = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        lib, dev = self._nvml, self._dev
+        if lib.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(mhz)) == 0:  # 1 = NVML_CLOCK_SM
+            self.sm.append(float(mhz.value))
+        if lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:
+            self.sm_max.append(float(mx.value))
+        if lib.nvmlDeviceGetCurrentClocksThrottleReasons(dev, ctypes.byref(r)) == 0:
+            for bit, name in self.REASONS.items():
+                if r.value & bit:
+                    self.reasons.add(name)
+
+    def _smi_sample(self):
+        out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+        if out.returncode != 0 or not out.stdout.strip():
+            return
+        f = [x.strip() for x in out.stdout.strip().split(",")]
+        if f[0].replace(".", "").isdigit():
+            self.sm.append(float(f[0]))
+        if f[1].replace(".", "").isdigit():
+            self.sm_max.append(float(f[1]))
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for i, name in enumerate(names):
+            if len(f) > 4 + i and f[4 + i] == "Active":
+                self.reasons.add(name)
 
     def _run(self):
+        period = 0.001 if self._nvml else 0.2
         while not self._stop.is_set():
             try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
-                if out.returncode == 0 and out.stdout.strip():
-                    self.samples.append([x.strip() for x in out.stdout.strip().split(",")])
+                self._nvml_sample() if self._nvml else self._smi_sample()
             except Exception:
                 pass
-            self._stop.wait(0.2)
+            self._stop.wait(period)
 
     def __enter__(self):
+        self.source = "nvml, 1 ms" if self._nvml else "nvidia-smi, 200 ms"
         self._thread = threading.Thread(target=self._run, daemon=True)
         self._thread.start()
         return self
@@ -123,14 +177,10 @@ class ClockSampler:
             self._thread.join(timeout=10)
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        smax = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if len(s) > 4 + i and s[4 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(self.samples)}
+        if not self.sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "source": self.source}
+        return {"sm_mhz": statistics.median(self.sm), "sm_max_mhz": max(self.sm_max) if self.sm_max else None,
+                "reasons": sorted(self.reasons), "samples": len(self.sm), "source": self.source}
 
 
 def build_workload(name: str) -> workloads.Workload:
@@ -225,6 +275,8 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         e1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall
+    if sampler:
+        sampler.__exit__(None, None, None)
     if world > 1:
         dist.barrier()
     # Split timing (after the timed region): the plan, then the select kernel(s).
@@ -236,8 +288,6 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         g_sel.replay()
         e2.record(stream)
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.__exit__(None, None, None)
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     plan_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev3]
     sel_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev3]
@@ -341,7 +391,9 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32 scores, u32 keys, i32 indices", "data": "synthetic (seeded)",
+        "vs_baseline": round(value / PAGES_GBS[name][0], 4) if name in PAGES_GBS else None,
+        "vs_baseline_source": PAGES_GBS[name][1] if name in PAGES_GBS else None,
+        "dtype": "f32 scores, u32 keys, i32 indices", "data": "synthetic (seeded)",
         "config": config_of(wl, name, world),
         "us_per_call": round(ms_step * 1e3, 2),
         "plan_us": round(statistics.mean(r["plan_ms"]) * 1e3, 2),
@@ -373,8 +425,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode")
-    ap.add_argument("--secondary", default="throughput,long1,long8,long32,ragged",
+    ap.add_argument("--workload", default="throughput",
+                    help="headline workload: batch 2048 x 64K, k=512, the shape the bandwidth figures are quoted on")
+    ap.add_argument("--secondary", default="decode,long1,long8,long32,ragged",
                     help="comma list of extra workloads timed after the headline one ('' for none)")
     args = ap.parse_args()
     world, rank, local = dist_env()
@@ -384,10 +437,12 @@ def main():
             return
         wl = build_workload(args.workload)
         times, last = [], None
+        # about two minutes of host work in all, whatever --steps is
+        per_step = max(0.5, min(8.0, 120.0 / max(1, args.steps)))
         for _ in range(args.warmup):
-            oracle_sample_time(wl, target_s=2.0)
+            oracle_sample_time(wl, target_s=min(2.0, per_step))
         for _ in range(args.steps):
-            last = oracle_sample_time(wl, target_s=8.0)
+            last = oracle_sample_time(wl, target_s=per_step)
             times.append(last["value"])
         v = statistics.mean(times)
         print(json.dumps({
@@ -413,7 +468,7 @@ def main():
     for name in [s for s in args.secondary.split(",") if s]:
         try:
             sub = gpu_line(name, max(3, args.steps // 2), max(3, args.warmup // 2), world, rank, local, full=False)
-            extra.append({k: sub[k] for k in ("config", "value", "us_per_call", "select_us", "plan_us",
+            extra.append({k: sub[k] for k in ("config", "value", "vs_baseline", "us_per_call", "select_us", "plan_us",
                                               "roofline", "device_flags")})
         except Exception as e:  # report, never hide
             extra.append({"workload": name, "error": repr(e)})

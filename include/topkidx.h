@@ -225,6 +225,8 @@ typedef struct {
     int32_t gate_fill_percent;          /* 0: automatic; else 1..100: the gate is loosened until it
                                            is expected to pass this share of the candidate buffer
                                            (never tighter than the sampling bound needs)         */
+    int32_t single_block_threads;       /* 0: automatic; 256 or 512: threads per block of the
+                                           single-block kernel on rows longer than 16K            */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -63,6 +63,7 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("candidate_capacity", ctypes.c_int32),
         ("samples", ctypes.c_int32),
         ("gate_fill_percent", ctypes.c_int32),
+        ("single_block_threads", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -26,6 +26,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Prefetches the 128-byte line holding `p` into L2 (no register result, no
+// fault on the access).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------- shared-memory accessors
 // Explicit .shared accesses on 32-bit shared-window addresses, so that hot
 // loops never fall back to generic loads, stores or atomics.  All carry a

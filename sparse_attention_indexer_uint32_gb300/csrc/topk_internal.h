@@ -140,9 +140,10 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
 // Host-side launchers (defined in topk_kernels.cu).
 cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
                         void* workspace, cudaStream_t stream);
-cudaError_t launch_select(const SelectParams& p, int cluster, int grid_units, size_t smem, cudaStream_t stream);
-cudaError_t select_occupancy(int cluster, size_t smem, int* units_out);
-int select_threads(int cluster);
+// threads: 256 or 512 per block when cluster == 1; 512 for clusters.
+cudaError_t launch_select(const SelectParams& p, int cluster, int threads, int grid_units, size_t smem,
+                          cudaStream_t stream);
+cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_out);
 cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
                                   int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream);
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream);

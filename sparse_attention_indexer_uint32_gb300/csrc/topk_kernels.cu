@@ -116,6 +116,32 @@ __device__ __forceinline__ int32_t page_map(const int32_t* pt_row, int32_t log2_
     return static_cast<int32_t>((page << log2_page) + (static_cast<uint32_t>(raw) & mask));
 }
 
+// Writes n results of a row: slot dst0 + q gets position src(q) (or -1) in
+// raw_row and its page-table mapping in out_row.  Four entries per thread are
+// in flight: their page-table loads are all issued before any store.
+template <int NT, typename Src>
+__device__ __forceinline__ void write_results(int32_t* out_row, int32_t* raw_row, const int32_t* pt_row,
+                                              int32_t log2_page, uint32_t n, uint32_t dst0, uint32_t tid, Src src) {
+    for (uint32_t q0 = tid; q0 < n; q0 += 4u * NT) {
+        int32_t r[4], v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t q = q0 + u * NT;
+            r[u] = q < n ? src(q) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = page_map(pt_row, log2_page, r[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t q = q0 + u * NT;
+            if (q < n) {
+                out_row[dst0 + q] = v[u];
+                if (raw_row) raw_row[dst0 + q] = r[u];
+            }
+        }
+    }
+}
+
 struct ScanResult {
     uint32_t bin, above, count, total;
     uint32_t local;  // this block's own count in `bin` (differs from `count` only in a cluster)
@@ -282,7 +308,7 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
 //     cluster_threshold": the transform is a separate pass).
 // ============================================================================
 template <int NT, int C>
-__global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const SelectParams p) {
+__global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const SelectParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Layout lay = make_layout(C, p.tile, p.stages, p.cap, p.k);
     const uint32_t sbase = ptx::smem_addr(smem_raw);
@@ -498,19 +524,26 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
 
             if (static_cast<uint32_t>(L) <= K) {
                 // Every position is selected (seq_len <= k): no select at all.
-                if (rank == 0) {
-                    for (uint32_t q = tid; q < K; q += NT) {
-                        const int32_t r = q < static_cast<uint32_t>(L) ? static_cast<int32_t>(q) : -1;
-                        out_row[q] = page_map(pt_row, p.log2_page, r);
-                        if (raw_row) raw_row[q] = r;
-                    }
-                }
+                if (rank == 0)
+                    write_results<NT>(out_row, raw_row, pt_row, p.log2_page, K, 0u, tid, [&](uint32_t q) {
+                        return q < static_cast<uint32_t>(L) ? static_cast<int32_t>(q) : -1;
+                    });
                 load_samples(j + 1);
                 continue;
             }
 
             uint32_t s0, s1;
             slice_of(L, s0, s1);
+            {
+                // Pull this slice's page-table entries into L2 now, so that the
+                // final gather finds them there.  Skipped when the slice spans
+                // far more pages than results (small pages).
+                const uint32_t pg0 = s0 >> p.log2_page;
+                const uint32_t npg = s1 > s0 ? ((s1 - 1u) >> p.log2_page) - pg0 + 1u : 0u;
+                if (npg > 0u && npg <= 8u * K)
+                    for (uint32_t e = 32u * tid; e < npg + 31u; e += 32u * NT)
+                        ptx::prefetch_l2(pt_row + pg0 + min(e, npg - 1u));
+            }
             const uint32_t ntiles = ptx::lds_u32(s.it_tiles + 4u * j);
             const float* row_ptr = p.scores + static_cast<int64_t>(row) * p.row_stride;
 
@@ -1029,11 +1062,9 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
             const uint32_t nemit = min(ptx::lds_u32(CTL(s, nemit)), K);
             if (C == 1) {
                 if (nemit != Kp && tid == 0) set_err(TOPK_FLAG_INTERNAL);
-                for (uint32_t q = tid; q < K; q += NT) {
-                    const int32_t r = q < nemit ? static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q)) : -1;
-                    out_row[q] = page_map(pt_row, p.log2_page, r);
-                    if (raw_row) raw_row[q] = r;
-                }
+                write_results<NT>(out_row, raw_row, pt_row, p.log2_page, K, 0u, tid, [&](uint32_t q) {
+                    return q < nemit ? static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q)) : -1;
+                });
             } else {
                 if (tid < C) ptx::st_cluster_u32(ptx::map_rank(CTL(s, rank_cnt) + 4u * rank, tid), nemit);
                 ptx::cluster_sync();
@@ -1044,14 +1075,10 @@ __global__ void __launch_bounds__(NT, C == 1 ? 3 : 2) select_kernel(const Select
                     total += c;
                 }
                 if (rank == 0 && tid == 0 && total != Kp) set_err(TOPK_FLAG_INTERNAL);
-                for (uint32_t q = tid; q < nemit; q += NT) {
-                    const uint32_t slot = before + q;
-                    if (slot < K) {
-                        const int32_t r = static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q));
-                        out_row[slot] = page_map(pt_row, p.log2_page, r);
-                        if (raw_row) raw_row[slot] = r;
-                    }
-                }
+                const uint32_t n_own = before < K ? min(nemit, K - before) : 0u;
+                write_results<NT>(out_row, raw_row, pt_row, p.log2_page, n_own, before, tid, [&](uint32_t q) {
+                    return static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q));
+                });
                 if (rank == 0) {
                     for (uint32_t q = total + tid; q < K; q += NT) {
                         out_row[q] = -1;
@@ -1133,13 +1160,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
         uint32_t* c = &cnt[0][0];
         for (int i = tid; i < kPlanKeys * kPlanWarps; i += kPlanThreads) c[i] = 0;
         __syncthreads();
+        // All loads are issued before any is used (indices clamped into the
+        // batch rather than branched around), so their latencies overlap.
+        int32_t len[kPlanPerThread];
+#pragma unroll
+        for (int q = 0; q < kPlanPerThread; ++q)
+            len[q] = __ldg(seq_lens + min(base + q * kPlanThreads + tid, batch - 1));
         uint32_t key[kPlanPerThread];
 #pragma unroll
         for (int q = 0; q < kPlanPerThread; ++q) {
             const int32_t b = base + q * kPlanThreads + tid;
             key[q] = 0xffffffffu;
             if (b < batch) {
-                const int32_t L = clamp_len(__ldg(seq_lens + b), max_seq_len, &flags);
+                const int32_t L = clamp_len(len[q], max_seq_len, &flags);
                 key[q] = static_cast<uint32_t>((L > threshold ? 64 : 0) + length_bucket(L));
             }
         }
@@ -1338,11 +1371,12 @@ cudaError_t launch_plain(void (*kern)(Args...), dim3 grid, dim3 block, cudaStrea
 
 }  // namespace
 
-int select_threads(int cluster) { return cluster == 1 ? 256 : 512; }
-
-cudaError_t launch_select(const SelectParams& p, int cluster, int grid_units, size_t smem, cudaStream_t stream) {
+cudaError_t launch_select(const SelectParams& p, int cluster, int threads, int grid_units, size_t smem,
+                          cudaStream_t stream) {
     switch (cluster) {
-        case 1: return launch_select_t<256, 1>(p, grid_units, smem, stream);
+        case 1:
+            return threads == 512 ? launch_select_t<512, 1>(p, grid_units, smem, stream)
+                                  : launch_select_t<256, 1>(p, grid_units, smem, stream);
         case 2: return launch_select_t<512, 2>(p, grid_units, smem, stream);
         case 4: return launch_select_t<512, 4>(p, grid_units, smem, stream);
         case 8: return launch_select_t<512, 8>(p, grid_units, smem, stream);
@@ -1351,9 +1385,10 @@ cudaError_t launch_select(const SelectParams& p, int cluster, int grid_units, si
     }
 }
 
-cudaError_t select_occupancy(int cluster, size_t smem, int* units_out) {
+cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_out) {
     switch (cluster) {
-        case 1: return occupancy_t<256, 1>(smem, units_out);
+        case 1:
+            return threads == 512 ? occupancy_t<512, 1>(smem, units_out) : occupancy_t<256, 1>(smem, units_out);
         case 2: return occupancy_t<512, 2>(smem, units_out);
         case 4: return occupancy_t<512, 4>(smem, units_out);
         case 8: return occupancy_t<512, 8>(smem, units_out);

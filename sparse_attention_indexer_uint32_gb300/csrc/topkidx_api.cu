@@ -35,7 +35,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: 8, the cluster size both the PR and the
 // DistRadixTopK README use.
-topk_tuning_t g_tuning = {32768, 65536, 15, 8, 0, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 8, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -68,6 +68,7 @@ int32_t long_threshold(const topk_tuning_t& t, int32_t batch) {
 
 struct PathConfig {
     int cluster;
+    int threads;
     int tile;
     int stages;
     int cap;
@@ -98,6 +99,10 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
     // cluster rows, 16 KB otherwise (short rows keep 3 blocks per SM).
     c.tile = (few_rows || (cluster == 1 && max_seq_len > 16384)) ? 8192 : 4096;
     c.stages = cluster == 1 ? 2 : (few_rows ? 5 : 3);
+    // Threads per block: clusters 512; single blocks 256 (three blocks per SM
+    // on short rows), or 512 on long rows when asked.
+    c.threads = 512;
+    if (cluster == 1) c.threads = (t.single_block_threads == 512 && c.tile == 8192) ? 512 : 256;
     int cap = t.candidate_capacity;
     if (cap == 0) {
         cap = cluster == 1 ? 4 * k : k;
@@ -120,11 +125,11 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
 }
 
 // Resident units (blocks, or clusters) of the select kernel for a launch shape.
-topk_status_t resident_units(int cluster, size_t smem, int* units) {
+topk_status_t resident_units(int cluster, int threads, size_t smem, int* units) {
     static std::map<std::pair<int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_pair(cluster * 64 + dev, smem);
+    const auto key = std::make_pair((threads * 64 + cluster) * 64 + dev, smem);
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         auto it = cache.find(key);
@@ -134,7 +139,7 @@ topk_status_t resident_units(int cluster, size_t smem, int* units) {
         }
     }
     int u = 0;
-    const cudaError_t e = select_occupancy(cluster, smem, &u);
+    const cudaError_t e = select_occupancy(cluster, threads, smem, &u);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (u <= 0) {
         snprintf(g_last_error, sizeof(g_last_error), "select kernel (cluster %d, %zu B smem) cannot be resident",
@@ -185,6 +190,8 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (t->samples != 0 && (t->samples < 32 || t->samples > kMaxSamples || t->samples % 32 != 0))
         return TOPK_EINVAL;
     if (t->gate_fill_percent < 0 || t->gate_fill_percent > 100) return TOPK_EINVAL;
+    if (t->single_block_threads != 0 && t->single_block_threads != 256 && t->single_block_threads != 512)
+        return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -252,7 +259,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     if (launch_long) {
         const PathConfig c = path_config(t.cluster_size, k, batch, max_seq_len, t);
         int units = 0;
-        const topk_status_t r = resident_units(c.cluster, c.smem, &units);
+        const topk_status_t r = resident_units(c.cluster, c.threads, c.smem, &units);
         if (r != TOPK_OK) return r;
         SelectParams q = p;
         q.items = plan_long_list(workspace);
@@ -263,13 +270,13 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         q.samples = c.samples;
         q.gate_fill = c.gate_fill;
         const int grid = batch < units ? batch : units;
-        const cudaError_t e = launch_select(q, c.cluster, grid, c.smem, st);
+        const cudaError_t e = launch_select(q, c.cluster, c.threads, grid, c.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
     }
     {
         const PathConfig c = path_config(1, k, batch, max_seq_len, t);
         int units = 0;
-        const topk_status_t r = resident_units(1, c.smem, &units);
+        const topk_status_t r = resident_units(1, c.threads, c.smem, &units);
         if (r != TOPK_OK) return r;
         SelectParams q = p;
         q.items = plan_short_list(workspace, batch);
@@ -287,7 +294,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         // same number of rows when all rows are short.
         const int per_unit = (batch + units - 1) / units;
         const int grid = (batch + per_unit - 1) / per_unit;
-        const cudaError_t e = launch_select(q, 1, grid, c.smem, st);
+        const cudaError_t e = launch_select(q, 1, c.threads, grid, c.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "select launch");
     }
     return TOPK_OK;

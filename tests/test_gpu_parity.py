@@ -131,6 +131,16 @@ def test_gate_fill_extremes(fill, cluster):
     compare(wl, out, raw)
 
 
+@pytest.mark.parametrize("dist", ["normal", "bf16"])
+def test_single_block_512_threads(dist):
+    """The 512-thread single-block kernel on rows over 16K (ragged tail,
+    short rows and ties included)."""
+    wl = workloads.random_case(seed=470, batch=40, min_len=0, max_len=150001, k=1000, page_size=32, dist=dist)
+    with tuning(single_block_threads=512, long_threshold=1 << 30, long_threshold_small_batch=1 << 30):
+        out, raw, _ = run_gpu(wl)
+    compare(wl, out, raw)
+
+
 def test_trend_rows_cluster():
     """Rows with a positional trend (the gate's sample must not alias)."""
     wl = workloads.long_context(batch=2, seq_len=300000)
