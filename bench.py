@@ -183,15 +183,17 @@ class ClockSampler:
                 "reasons": sorted(self.reasons), "samples": len(self.sm), "source": self.source}
 
 
-def build_workload(name: str) -> workloads.Workload:
+def build_workload(name: str, shard: int = 0) -> workloads.Workload:
+    """The named workload; shard r (rank r of a multi-GPU run) draws its own
+    batch of the same shape from its own seed."""
     if name == "decode":
-        return workloads.decode()
+        return workloads.decode(shard=shard)
     if name == "throughput":
-        return workloads.throughput()
+        return workloads.throughput(shard=shard)
     if name.startswith("long"):
-        return workloads.long_context(int(name[4:] or 1))
+        return workloads.long_context(int(name[4:] or 1), shard=shard)
     if name == "ragged":
-        return workloads.ragged()
+        return workloads.ragged(shard=shard)
     if name == "tiny":
         return workloads.tiny()
     raise ValueError(name)
@@ -201,9 +203,28 @@ def config_of(wl: workloads.Workload, name: str, world: int) -> dict:
     eff = np.clip(wl.seq_lens.astype(np.int64), 0, wl.max_seq_len)
     return {"workload": wl.name, "kind": name, "batch": wl.batch, "seq_len": int(eff.max()),
             "sum_seq_len": int(eff.sum()), "k": wl.k, "page_size": wl.page_size, "row_stride": wl.row_stride,
-            "raw_output": wl.want_raw, "global_batch": wl.batch * world, "parallelism": f"replica{world}",
+            "raw_output": wl.want_raw, "global_batch": wl.batch * world, "parallelism": f"dp{world}",
+            "sharding": "each rank selects its own batch of this shape; no collective on the data path",
             "l2": "flushed between timed steps (256 MB write); inputs > L2 for decode/throughput",
             "launch": "plan and transform replayed from CUDA graphs; events on the launching stream"}
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest value of x over all ranks (x itself on one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, world: int, steps: int, total_ms_max: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed over the slowest
+    rank's time for the timed steps."""
+    return bytes_per_rank_step * world * steps / (total_ms_max / 1e3) / 1e9
 
 
 def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: bool):
@@ -291,11 +312,7 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     plan_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev3]
     sel_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev3]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     flags = _lib.topk_read_flags(ws)
     res = {"total_ms": total_ms, "step_ms": step_ms, "plan_ms": plan_ms, "select_ms": sel_ms,
            "wall_s": t_wall, "flags": flags, "launches_per_step": launches_per_step,
@@ -379,14 +396,14 @@ def oracle_sample_time(wl, target_s: float = 12.0):
 
 def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: int, full: bool):
     log("workload", name)
-    wl = build_workload(name)
+    wl = build_workload(name, shard=rank)
     nbytes = wl.algorithmic_bytes()
     r = time_gpu(wl, steps, warmup, local, world, want_clocks=full)
     log("timed", name, f"{r['total_ms'] / steps:.4f} ms/step", "flags", r["flags"])
     peak, peak_kind = measured_peak()
     ms_step = r["total_ms"] / steps
     sel_avg = statistics.mean(r["select_ms"])
-    value = nbytes * world * steps / (r["total_ms"] / 1e3) / 1e9
+    value = job_gbs(nbytes, world, steps, r["total_ms"])
     achieved = nbytes / (sel_avg / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
@@ -410,8 +427,12 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
         e2e_steps = max(3, min(steps, 10))
         ms, h2d, d2h = time_e2e(wl, e2e_steps, 2, local)
         log("e2e", f"{ms:.3f} ms/step")
-        line["e2e"] = {"value": round(nbytes / (ms / 1e3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+        import torch
+
+        ms = max_over_ranks(ms, world, torch.device("cuda", local))
+        line["e2e"] = {"value": round(job_gbs(nbytes, world, 1, ms), 2), "unit": "GB/s",
+                       "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
+                       "ms_per_step": round(ms, 4)}
         line["clocks"] = r["clocks"]
         if rank == 0 and world == 1:
             line["cpu_baseline"] = oracle_sample_time(wl)

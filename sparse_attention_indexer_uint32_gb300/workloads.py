@@ -69,8 +69,13 @@ class Workload:
         return int(4 * eff.sum() + 4 * self.batch + 4 * self.batch * self.k * outputs)
 
 
-def _rng(tag: int) -> np.random.Generator:
-    return np.random.default_rng(BASE_SEED + tag)
+# Seed offset between shards: shard r of a workload (one per process when
+# several GPUs each run their own batch) draws from tag + SHARD_STRIDE * r.
+SHARD_STRIDE = 7919
+
+
+def _rng(tag: int, shard: int = 0) -> np.random.Generator:
+    return np.random.default_rng(BASE_SEED + tag + SHARD_STRIDE * shard)
 
 
 def _normal_f32(rng: np.random.Generator, shape) -> np.ndarray:
@@ -105,16 +110,17 @@ def tiny() -> Workload:
                     identity_table(B, pages_for(L, 64)), 64, 512, L, want_raw=True)
 
 
-def decode(batch: int = 8192, seq_len: int = 8192) -> Workload:
-    rng = _rng(2)
+def decode(batch: int = 8192, seq_len: int = 8192, shard: int = 0) -> Workload:
+    rng = _rng(2, shard)
     scores = _normal_f32(rng, (batch, seq_len))
     table = permuted_table(rng, batch, pages_for(seq_len, 64))
     return Workload(f"decode_{batch}x{seq_len}_k512", scores, np.full(batch, seq_len, np.int32),
                     table, 64, 512, seq_len)
 
 
-def throughput(batch: int = 2048, seq_len: int = 65536, dim: int = 128, chunk: int = 256) -> Workload:
-    rng = _rng(3)
+def throughput(batch: int = 2048, seq_len: int = 65536, dim: int = 128, chunk: int = 256,
+               shard: int = 0) -> Workload:
+    rng = _rng(3, shard)
     q = _normal_f32(rng, (batch, dim)).astype(np.float64)
     kmat = _normal_f32(rng, (seq_len, dim)).astype(np.float64)
     scores = np.empty((batch, seq_len), dtype=np.float32)
@@ -126,8 +132,8 @@ def throughput(batch: int = 2048, seq_len: int = 65536, dim: int = 128, chunk: i
                     table, 64, 512, seq_len)
 
 
-def long_context(batch: int = 1, seq_len: int = 1 << 20) -> Workload:
-    rng = _rng(4)
+def long_context(batch: int = 1, seq_len: int = 1 << 20, shard: int = 0) -> Workload:
+    rng = _rng(4, shard)
     trend = 0.5 * np.sin(2.0 * math.pi * np.arange(seq_len, dtype=np.float64) / 4096.0)
     scores = np.empty((batch, seq_len), dtype=np.float32)
     for b in range(batch):
@@ -143,8 +149,8 @@ RAGGED_HALF_NEG_INF = (20, 60, 100, 121)
 RAGGED_FORCED = {20: 1500}
 
 
-def ragged(batch: int = 128, max_len: int = 262144, min_len: int = 1024) -> Workload:
-    rng = _rng(5)
+def ragged(batch: int = 128, max_len: int = 262144, min_len: int = 1024, shard: int = 0) -> Workload:
+    rng = _rng(5, shard)
     lens = rng.integers(min_len, max_len, size=batch, endpoint=True).astype(np.int32)
     for b, L in {**RAGGED_SHORT, **RAGGED_FORCED}.items():
         if b < batch:
