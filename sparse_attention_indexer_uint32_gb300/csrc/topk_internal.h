@@ -29,7 +29,9 @@ struct PlanHeader {
     int32_t n_long;
     int32_t n_short;
     uint32_t flags;
-    int32_t reserved[9];
+    int32_t identity;  // 1: every row has the same class and length bucket, so the
+                       // one non-empty list is rows 0..batch-1 in order (not written)
+    int32_t reserved[8];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
@@ -81,12 +83,13 @@ struct __align__(16) Control {
     uint32_t nfin;        // entries in the finish list
     uint32_t smax;        // largest sample key
     uint32_t res_bin, res_above, res_count, res_total;  // result of the last histogram scan
-    uint32_t rank_cnt[kMaxCluster];  // per-rank emitted counts (output placement)
     uint32_t rank_eq[kMaxCluster];   // per-rank copies of the threshold key (tie quotas)
     uint32_t err;
     uint32_t res_local;   // the local (un-merged) count of the bin found by the last scan
     uint32_t win_tiles;   // bulk-copy tiles in the current window of work items
-    uint32_t pad[1];
+    uint32_t out_cursor[2];  // rank 0 of a cluster: output slots handed out, by row parity
+    uint32_t out_base;       // this block's first output slot of the current row
+    uint32_t pad[2];
 };
 
 struct Layout {

@@ -23,6 +23,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 #include "topk_internal.h"
@@ -65,6 +66,28 @@ __device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t v, int lane) {
         if (lane >= o) v += t;
     }
     return v;
+}
+
+// Exclusive prefix sum and total over the warp of small per-lane counts
+// (0..32), from bit-plane ballots: no dependent shuffle chain.  Only the
+// planes up to the warp's largest count are taken (one or two when the gate
+// is sparse).
+struct WarpPrefix {
+    uint32_t excl, total;
+};
+__device__ __forceinline__ WarpPrefix warp_prefix_small(uint32_t cnt, int lane) {
+    const uint32_t lt = (1u << lane) - 1u;
+    WarpPrefix r{0u, 0u};
+    const int planes = 32 - __clz(__reduce_max_sync(kFull, cnt));
+#pragma unroll
+    for (int b = 0; b < 6; ++b) {
+        if (b < planes) {
+            const uint32_t bal = __ballot_sync(kFull, (cnt >> b) & 1u);
+            r.excl += static_cast<uint32_t>(__popc(bal & lt)) << b;
+            r.total += static_cast<uint32_t>(__popc(bal)) << b;
+        }
+    }
+    return r;
 }
 
 // Warp-wide bitonic compare-and-swap sort, largest value to lane 0
@@ -335,7 +358,6 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     s.ctl_ptr = reinterpret_cast<Control*>(smem_raw + lay.ctl);
 
     constexpr int kSamplesPerThread = kMaxSamples / NT;
-    constexpr int kMaxVecPerTile = 8;  // float4s per thread per bulk-copy tile, at most (mask is 32 bits)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = (C > 1) ? ptx::cluster_ctarank() : 0u;
     const uint32_t unit = (C > 1) ? ptx::cluster_id_x() : blockIdx.x;
@@ -356,6 +378,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         ptx::sts_u32(CTL(s, nfin), 0);
         ptx::sts_u32(CTL(s, smax), 0);
         ptx::sts_u32(CTL(s, err), 0);
+        ptx::sts_u32(CTL(s, out_cursor[0]), 0);
+        ptx::sts_u32(CTL(s, out_cursor[1]), 0);
         for (uint32_t i = 0; i < stages; ++i) ptx::sts_u32(s.claim + 4u * i, 0xffffffffu);
     }
     clear_hist<NT>(s.hist_a, tid);
@@ -372,6 +396,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         return;  // same for every block of a cluster
     }
     const int32_t n_first = min(p.n_items_dev ? *p.n_items_dev : p.n_items_host, p.batch);
+    const bool identity = p.plan && p.plan->identity;  // the plan wrote no lists: item i is row i
     const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
     const int32_t n_items = n_first + max(n_second, 0);
     const int32_t my_items = n_items > static_cast<int32_t>(unit)
@@ -391,6 +416,11 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     // Consumer tile sequence number (the same in every thread); tile t of the
     // sequence lives in ring stage t % stages.
     uint32_t cseq = 0;
+    // Cluster rows that reached the output step, and (rank 0, thread 0) the
+    // last such row's k: row e takes its output slots from rank 0's
+    // out_cursor[e & 1], which rank 0 checks and clears after the next row's
+    // histogram merge (every rank is past row e's output by then).
+    uint32_t erow = 0, prev_kp = 0;
 
     auto slice_of = [&](int32_t L, uint32_t& s0, uint32_t& s1) {
         const uint32_t chunk = ((static_cast<uint32_t>(L) + C - 1) / C + 3u) & ~3u;
@@ -402,7 +432,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         const int32_t nw = min(kItemsMax, my_items - w0);
         for (int32_t i = tid; i < nw; i += NT) {
             const int32_t it = static_cast<int32_t>(unit) + (w0 + i) * static_cast<int32_t>(nunits);
-            const int32_t row = it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first];
+            const int32_t row = identity ? (it < n_first ? it : it - n_first)
+                                         : (it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first]);
             int32_t L = -1;
             uint32_t nt = 0;
             if (row < 0 || row >= p.batch) {  // a list that does not belong to this batch
@@ -616,40 +647,40 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
 
             // ------------------------------------------------- 2. pass 1
             const bool buffering = !p.force_two_pass;
-            for (uint32_t t = 0; t < ntiles; ++t) {
-                const uint32_t st = cseq % stages;
-                const bool gave_up = (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) != 0u;
-                if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns))
-                    set_err(TOPK_FLAG_TIMEOUT);
-                const uint32_t off = t * tile;
-                const uint32_t n4 = ((s1 + 3u) & ~3u) - s0;
-                const uint32_t nvec = min(tile, n4 - off) >> 2;
-                const uint32_t ring_st = s.ring + st * tile * 4u;
-                const uint32_t base_idx = s0 + off;
-                // Each thread tests float4s v = q * NT + tid of the tile against the
-                // gate into a bitmask with one float compare per element: with f_lo
-                // the float whose key is lo, !(x < f_lo) holds for every x with
-                // key(x) >= lo, and also for NaNs (and everything, if f_lo is a NaN).
-                // One warp-wide reservation per tile; only the gated elements, a
-                // small fraction, are re-read, keyed exactly, counted in the
-                // histogram and buffered.  A false positive (a NaN under the gate)
-                // fills its reserved slot with key 0, which no later step selects.
-                const uint32_t lim = min(s1 - base_idx, tile);  // valid elements in this tile
-                uint32_t gmask = 0;
-                if (lim == tile) {
-#pragma unroll
-                    for (int q = 0; q < kMaxVecPerTile; ++q) {
-                        if (q < static_cast<int>(vec_per_tile)) {
-                            const float4 x = ptx::lds_f4(ring_st + 16u * (q * NT + tid));
-                            gmask |= ((x.x < f_lo ? 0u : 1u) | (x.y < f_lo ? 0u : 2u) | (x.z < f_lo ? 0u : 4u) |
-                                      (x.w < f_lo ? 0u : 8u))
+            // The tile loop, compiled for V float4s per thread per tile (the
+            // tile and block sizes in use give V = 2, 4 or 8).
+            auto pass1 = [&](auto v_tag) {
+                constexpr int V = decltype(v_tag)::value;
+                for (uint32_t t = 0; t < ntiles; ++t) {
+                    const uint32_t st = cseq % stages;
+                    const bool gave_up = (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) != 0u;
+                    if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns))
+                        set_err(TOPK_FLAG_TIMEOUT);
+                    const uint32_t off = t * tile;
+                    const uint32_t ring_st = s.ring + st * tile * 4u;
+                    const uint32_t base_idx = s0 + off;
+                    // Each thread tests float4s v = q * NT + tid of the tile against the
+                    // gate into a bitmask with one float compare per element: with f_lo
+                    // the float whose key is lo, !(x < f_lo) holds for every x with
+                    // key(x) >= lo, and also for NaNs (and everything, if f_lo is a NaN).
+                    // One warp-wide reservation per tile; only the gated elements, a
+                    // small fraction, are re-read, keyed exactly, counted in the
+                    // histogram and buffered.  A false positive (a NaN under the gate)
+                    // fills its reserved slot with key 0, which no later step selects.
+                    const uint32_t lim = min(s1 - base_idx, tile);  // valid elements in this tile
+                    uint32_t gmask = 0;
+                    if (lim == tile) {
+                        float4 x[V];
+    #pragma unroll
+                        for (int q = 0; q < V; ++q) x[q] = ptx::lds_f4(ring_st + 16u * (q * NT + tid));
+    #pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            gmask |= ((x[q].x < f_lo ? 0u : 1u) | (x[q].y < f_lo ? 0u : 2u) | (x[q].z < f_lo ? 0u : 4u) |
+                                      (x[q].w < f_lo ? 0u : 8u))
                                      << (4 * q);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < kMaxVecPerTile; ++q) {
-                        if (q < static_cast<int>(vec_per_tile)) {
+                    } else {
+    #pragma unroll
+                        for (int q = 0; q < V; ++q) {
                             const uint32_t v = q * NT + tid;
                             const float4 x = ptx::lds_f4(ring_st + 16u * v);
                             const uint32_t e0 = 4u * v;
@@ -660,55 +691,76 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             gmask |= (g & valid) << (4 * q);
                         }
                     }
-                }
-                // Gated elements: each lane writes only the positions of its gated
-                // elements into its reserved slots; the warp then takes the
-                // compacted slots one per lane to key them exactly, count them in
-                // the histogram and fill in their keys.  When the buffer is full (or
-                // not used) each lane counts its own elements instead.
-                const uint32_t cnt = __popc(gmask);
-                const uint32_t incl = warp_inclusive_sum(cnt, lane);
-                const uint32_t total = __shfl_sync(kFull, incl, 31);
-                uint32_t wbase = 0;
-                if (buffering && lane == 31 && total != 0u) wbase = ptx::atom_add_s(CTL(s, ncand), total);
-                wbase = __shfl_sync(kFull, wbase, 31);
-                if (buffering && wbase + total <= cap) {
-                    uint32_t slot = wbase + incl - cnt;
-                    while (gmask) {
-                        const int e = __ffs(gmask) - 1;
-                        gmask &= gmask - 1u;
-                        const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
-                        ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
-                        ++slot;
+                    // Gated elements: each lane writes only the positions of its gated
+                    // elements into its reserved slots; the warp then takes the
+                    // compacted slots one per lane to key them exactly, count them in
+                    // the histogram and fill in their keys.  When the buffer is full (or
+                    // not used) each lane counts its own elements instead.
+                    const uint32_t cnt = __popc(gmask);
+                    const WarpPrefix wp = warp_prefix_small(cnt, lane);
+                    const uint32_t total = wp.total;
+                    uint32_t wbase = 0;
+                    if (buffering && lane == 0 && total != 0u) wbase = ptx::atom_add_s(CTL(s, ncand), total);
+                    wbase = __shfl_sync(kFull, wbase, 0);
+                    if (buffering && wbase + total <= cap) {
+                        uint32_t slot = wbase + wp.excl;
+                        while (gmask) {
+                            const int e = __ffs(gmask) - 1;
+                            gmask &= gmask - 1u;
+                            const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
+                            ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
+                            ++slot;
+                        }
+                        __syncwarp();
+                        for (uint32_t i = lane; i < total; i += 32) {
+                            const uint32_t sl = wbase + i;
+                            const uint32_t idx_in_tile = ptx::lds_u32(s.cand_idx + 4u * sl) - base_idx;
+                            const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
+                            const bool pass = key >= lo;
+                            if (pass)
+                                ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
+                                               1u);
+                            ptx::sts_u32(s.cand_key + 4u * sl, pass ? key : 0u);
+                        }
+                    } else {
+                        // Runs of one bin within a lane take one atomic (a flat row
+                        // puts every element in the same bin).
+                        uint32_t run_bin = 0u, run_n = 0u;
+                        while (gmask) {
+                            const int e = __ffs(gmask) - 1;
+                            gmask &= gmask - 1u;
+                            const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
+                            const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
+                            if (key >= lo) {
+                                const uint32_t bin = min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1));
+                                if (bin != run_bin && run_n) {
+                                    ptx::red_add_s(s.hist_a + 4u * run_bin, run_n);
+                                    run_n = 0u;
+                                }
+                                run_bin = bin;
+                                ++run_n;
+                            }
+                        }
+                        if (run_n) ptx::red_add_s(s.hist_a + 4u * run_bin, run_n);
                     }
                     __syncwarp();
-                    for (uint32_t i = lane; i < total; i += 32) {
-                        const uint32_t sl = wbase + i;
-                        const uint32_t idx_in_tile = ptx::lds_u32(s.cand_idx + 4u * sl) - base_idx;
-                        const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
-                        const bool pass = key >= lo;
-                        if (pass)
-                            ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
-                                           1u);
-                        ptx::sts_u32(s.cand_key + 4u * sl, pass ? key : 0u);
+                    if (lane == 0) {
+                        ptx::mbar_arrive(&s.empty[st]);
+                        refill_after(cseq);
                     }
-                } else {
-                    while (gmask) {
-                        const int e = __ffs(gmask) - 1;
-                        gmask &= gmask - 1u;
-                        const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
-                        const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
-                        if (key >= lo)
-                            ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
-                                           1u);
-                    }
+                    ++cseq;
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(&s.empty[st]);
-                    refill_after(cseq);
-                }
-                ++cseq;
+            };
+            if (NT == 256) {
+                if (vec_per_tile == 8u)
+                    pass1(std::integral_constant<int, 8>{});
+                else
+                    pass1(std::integral_constant<int, 4>{});
+            } else {
+                if (vec_per_tile == 4u)
+                    pass1(std::integral_constant<int, 4>{});
+                else
+                    pass1(std::integral_constant<int, 2>{});
             }
             __syncthreads();
 
@@ -718,6 +770,11 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 if (tid == 0) ptx::sts_u32(s.hist_a + 4u * kSlotOverflow, local_ovf);
                 cluster_merge<NT, C>(s, s.hist_a, rank, tid);
                 hm = s.hist_m;
+                if (rank == 0 && tid == 0) {
+                    const uint32_t a = CTL(s, out_cursor[0]) + 4u * ((erow + 1u) & 1u);
+                    if (erow > 0u && ptx::lds_u32(a) != prev_kp) set_err(TOPK_FLAG_INTERNAL);
+                    ptx::sts_u32(a, 0u);
+                }
             }
             const bool overflow = (C > 1) ? (ptx::lds_u32(hm + 4u * kSlotOverflow) != 0u) : (local_ovf != 0u);
             ScanResult sr = scan_find<NT>(s, hm, Kp, tid, s.hist_a);
@@ -855,6 +912,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             const uint32_t v = v0 + u * NT;
                             xv[u] = v < nvec_slice ? __ldg(slice4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
+                        uint32_t run_bin = 0u, run_n = 0u;  // runs of one bin: one atomic
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const uint32_t v = v0 + u * NT;
@@ -863,10 +921,18 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             for (int c = 0; c < 4; ++c) {
                                 const uint32_t idx = s0 + 4u * v + c;
                                 const uint32_t key = score_key(xs[c]);
-                                if (v < nvec_slice && idx < s1 && key >= r_lo && key <= r_hi)
-                                    ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
+                                if (v < nvec_slice && idx < s1 && key >= r_lo && key <= r_hi) {
+                                    const uint32_t bin = (key - r_lo) >> sh;
+                                    if (bin != run_bin && run_n) {
+                                        ptx::red_add_s(h_next + 4u * run_bin, run_n);
+                                        run_n = 0u;
+                                    }
+                                    run_bin = bin;
+                                    ++run_n;
+                                }
                             }
                         }
+                        if (run_n) ptx::red_add_s(h_next + 4u * run_bin, run_n);
                     }
                 }
                 __syncthreads();
@@ -971,9 +1037,15 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 } else {
                     // Final streaming pass: > T is taken; copies of T up to the quota,
                     // in position order when only some of them are taken.
+                    // With nothing above T anywhere (G == 0: a flat or top-tied row),
+                    // a block that takes no copies skips the pass, and one that takes
+                    // some stops as soon as its quota is met.
                     const bool ordered = (!all_eq && quota > 0);
+                    const bool none_above = (G == 0u);
+                    const uint32_t vend = (none_above && !all_eq && quota == 0u) ? 0u : nvec_slice;
                     uint32_t running = 0;
-                    for (uint32_t vb = 0; vb < nvec_slice; vb += NT) {
+                    for (uint32_t vb = 0; vb < vend; vb += NT) {
+                        if (none_above && ordered && running >= quota) break;  // block-uniform
                         const uint32_t v = vb + tid;
                         uint32_t eqm = 0;
                         const bool in = v < nvec_slice;
@@ -1066,25 +1138,27 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     return q < nemit ? static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q)) : -1;
                 });
             } else {
-                if (tid < C) ptx::st_cluster_u32(ptx::map_rank(CTL(s, rank_cnt) + 4u * rank, tid), nemit);
-                ptx::cluster_sync();
-                uint32_t before = 0, total = 0;
-                for (uint32_t q = 0; q < static_cast<uint32_t>(C); ++q) {
-                    const uint32_t c = ptx::lds_u32(CTL(s, rank_cnt) + 4u * q);
-                    before += (q < rank) ? c : 0u;
-                    total += c;
-                }
-                if (rank == 0 && tid == 0 && total != Kp) set_err(TOPK_FLAG_INTERNAL);
-                const uint32_t n_own = before < K ? min(nemit, K - before) : 0u;
+                // Output slots come from one atomic on rank 0's cursor (no
+                // cluster barrier); all ranks together emit exactly Kp.
+                if (tid == 0)
+                    ptx::sts_u32(CTL(s, out_base),
+                                 ptx::atom_add_cluster_u32(
+                                     ptx::map_rank(CTL(s, out_cursor[0]) + 4u * (erow & 1u), 0), nemit));
+                __syncthreads();
+                const uint32_t before = ptx::lds_u32(CTL(s, out_base));
+                if (tid == 0 && before + nemit > Kp) set_err(TOPK_FLAG_INTERNAL);
+                const uint32_t n_own = before < Kp ? min(nemit, Kp - before) : 0u;
                 write_results<NT>(out_row, raw_row, pt_row, p.log2_page, n_own, before, tid, [&](uint32_t q) {
                     return static_cast<int32_t>(ptx::lds_u32(s.emit + 4u * q));
                 });
                 if (rank == 0) {
-                    for (uint32_t q = total + tid; q < K; q += NT) {
+                    for (uint32_t q = Kp + tid; q < K; q += NT) {
                         out_row[q] = -1;
                         if (raw_row) raw_row[q] = -1;
                     }
                 }
+                if (tid == 0) prev_kp = Kp;
+                ++erow;
             }
             __syncthreads();
         }
@@ -1098,10 +1172,18 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             const uint32_t r = ptx::lds_u32(s.claim + 4u * st);
             if (r != 0xffffffffu) ptx::mbar_wait_bounded(&s.full[st], r & 1u, p.timeout_ns);
         }
+    }
+    if (C > 1) {
+        ptx::cluster_sync();  // no block leaves while others may still address its shared memory
+        // every rank is past its last output: rank 0 checks the last row's slot count
+        if (rank == 0 && tid == 0 && erow > 0u &&
+            ptx::lds_u32(CTL(s, out_cursor[0]) + 4u * ((erow - 1u) & 1u)) != prev_kp)
+            set_err(TOPK_FLAG_INTERNAL);
+    }
+    if (tid == 0) {
         const uint32_t err = ptx::lds_u32(CTL(s, err));
         if (err) atomicOr(p.flags, err);
     }
-    if (C > 1) ptx::cluster_sync();  // no block leaves while others may still address its shared memory
 }
 
 namespace {
@@ -1148,13 +1230,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
     __shared__ uint32_t cnt[kPlanKeys][kPlanWarps];  // per-warp counts, then per-warp cursors
     __shared__ uint32_t warp_sum[kPlanWarps];
     __shared__ uint32_t flags_s;
+    __shared__ uint32_t uniform_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // The select kernel that follows waits for this grid's completion before
     // reading the lists, so it may be placed on the GPU right away.
     ptx::launch_dependents();
     int32_t* lists[2] = {plan_short_list(ws, batch), plan_long_list(ws)};
     uint32_t flags = 0;
-    if (tid == 0) flags_s = 0;
+    if (tid == 0) {
+        flags_s = 0;
+        uniform_s = 0;
+    }
+    // A batch that fits one sweep and whose rows all share one key needs no
+    // lists: the order is the identity, which the header says instead.
+    const bool one_sweep = batch <= kPlanThreads * kPlanPerThread;
     uint32_t n_long_total = 0;
     for (int32_t base = 0; base < batch; base += kPlanThreads * kPlanPerThread) {
         uint32_t* c = &cnt[0][0];
@@ -1210,6 +1299,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
             if (lane >= o) incl += t;
         }
         if (lane == 31) warp_sum[warp] = incl;
+        {
+            // the 8 lanes that own one key hold its whole count
+            uint32_t key_total = sum;
+            key_total += __shfl_xor_sync(kFull, key_total, 1);
+            key_total += __shfl_xor_sync(kFull, key_total, 2);
+            key_total += __shfl_xor_sync(kFull, key_total, 4);
+            if (one_sweep && (lane & 7) == 0 && key_total == static_cast<uint32_t>(batch)) uniform_s = 1;
+        }
         __syncthreads();
         uint32_t pre = 0, n_long = 0;
         for (int w = 0; w < kPlanWarps; ++w) {
@@ -1224,7 +1321,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
             run += v[u];
         }
         __syncthreads();
-        {
+        if (!uniform_s) {
             // Same runs: one atomic reserves a run's positions (run lengths are
             // counted backwards first).
             uint32_t rl[kPlanPerThread];
@@ -1258,6 +1355,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
         h->n_long = static_cast<int32_t>(n_long_total);
         h->n_short = batch - static_cast<int32_t>(n_long_total);
         h->flags = flags_s;
+        h->identity = uniform_s ? 1 : 0;
     }
 }
 
@@ -1369,30 +1467,37 @@ cudaError_t launch_plain(void (*kern)(Args...), dim3 grid, dim3 block, cudaStrea
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+template <int C>
+cudaError_t launch_select_c(const SelectParams& p, int threads, int grid_units, size_t smem, cudaStream_t stream) {
+    return threads == 512 ? launch_select_t<512, C>(p, grid_units, smem, stream)
+                          : launch_select_t<256, C>(p, grid_units, smem, stream);
+}
+template <int C>
+cudaError_t occupancy_c(int threads, size_t smem, int* units_out) {
+    return threads == 512 ? occupancy_t<512, C>(smem, units_out) : occupancy_t<256, C>(smem, units_out);
+}
+
 }  // namespace
 
 cudaError_t launch_select(const SelectParams& p, int cluster, int threads, int grid_units, size_t smem,
                           cudaStream_t stream) {
     switch (cluster) {
-        case 1:
-            return threads == 512 ? launch_select_t<512, 1>(p, grid_units, smem, stream)
-                                  : launch_select_t<256, 1>(p, grid_units, smem, stream);
-        case 2: return launch_select_t<512, 2>(p, grid_units, smem, stream);
-        case 4: return launch_select_t<512, 4>(p, grid_units, smem, stream);
-        case 8: return launch_select_t<512, 8>(p, grid_units, smem, stream);
-        case 16: return launch_select_t<512, 16>(p, grid_units, smem, stream);
+        case 1: return launch_select_c<1>(p, threads, grid_units, smem, stream);
+        case 2: return launch_select_c<2>(p, threads, grid_units, smem, stream);
+        case 4: return launch_select_c<4>(p, threads, grid_units, smem, stream);
+        case 8: return launch_select_c<8>(p, threads, grid_units, smem, stream);
+        case 16: return launch_select_c<16>(p, threads, grid_units, smem, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_out) {
     switch (cluster) {
-        case 1:
-            return threads == 512 ? occupancy_t<512, 1>(smem, units_out) : occupancy_t<256, 1>(smem, units_out);
-        case 2: return occupancy_t<512, 2>(smem, units_out);
-        case 4: return occupancy_t<512, 4>(smem, units_out);
-        case 8: return occupancy_t<512, 8>(smem, units_out);
-        case 16: return occupancy_t<512, 16>(smem, units_out);
+        case 1: return occupancy_c<1>(threads, smem, units_out);
+        case 2: return occupancy_c<2>(threads, smem, units_out);
+        case 4: return occupancy_c<4>(threads, smem, units_out);
+        case 8: return occupancy_c<8>(threads, smem, units_out);
+        case 16: return occupancy_c<16>(threads, smem, units_out);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -33,9 +33,10 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // Thresholds after SGLang PR #26788 (commit "Fuse the cluster/non-cluster
 // split for small batch": long rows above 32K for small batches, 64K
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
-// PR).  Blocks per long row: 8, the cluster size both the PR and the
-// DistRadixTopK README use.
-topk_tuning_t g_tuning = {32768, 65536, 15, 8, 0, 0, 0, 0, 0, 0};
+// PR).  Blocks per long row: chosen per call (cluster_size 0): 16 for one or
+// two rows, else 8, the cluster size both the PR and the DistRadixTopK README
+// use.
+topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -99,10 +100,13 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
     // cluster rows, 16 KB otherwise (short rows keep 3 blocks per SM).
     c.tile = (few_rows || (cluster == 1 && max_seq_len > 16384)) ? 8192 : 4096;
     c.stages = cluster == 1 ? 2 : (few_rows ? 5 : 3);
-    // Threads per block: clusters 512; single blocks 256 (three blocks per SM
-    // on short rows), or 512 on long rows when asked.
-    c.threads = 512;
-    if (cluster == 1) c.threads = (t.single_block_threads == 512 && c.tile == 8192) ? 512 : 256;
+    // Threads per block: single blocks 256 (three blocks per SM on short
+    // rows), or 512 on long rows when asked; clusters 512 when few rows pull
+    // 32 KB copies, else 256 (more float4s per thread per copy).
+    if (cluster == 1)
+        c.threads = (t.single_block_threads == 512 && c.tile == 8192) ? 512 : 256;
+    else
+        c.threads = few_rows ? 512 : 256;
     int cap = t.candidate_capacity;
     if (cap == 0) {
         cap = cluster == 1 ? 4 * k : k;
@@ -182,7 +186,8 @@ topk_status_t topk_get_tuning(topk_tuning_t* tuning_host) {
 topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (!t) return TOPK_EINVAL;
     if (t->long_threshold_small_batch < 0 || t->long_threshold < 0 || t->small_batch_max < 0) return TOPK_EINVAL;
-    if (t->cluster_size != 2 && t->cluster_size != 4 && t->cluster_size != 8 && t->cluster_size != 16)
+    if (t->cluster_size != 0 && t->cluster_size != 2 && t->cluster_size != 4 && t->cluster_size != 8 &&
+        t->cluster_size != 16)
         return TOPK_EINVAL;
     if (t->candidate_capacity != 0 &&
         (t->candidate_capacity < 2048 || t->candidate_capacity > 16384 || t->candidate_capacity % 64 != 0))
@@ -256,23 +261,9 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     p.timeout_ns = 2000000000ull;
 
     const bool launch_long = max_seq_len > threshold;
-    if (launch_long) {
-        const PathConfig c = path_config(t.cluster_size, k, batch, max_seq_len, t);
-        int units = 0;
-        const topk_status_t r = resident_units(c.cluster, c.threads, c.smem, &units);
-        if (r != TOPK_OK) return r;
-        SelectParams q = p;
-        q.items = plan_long_list(workspace);
-        q.n_items_dev = &hdr->n_long;
-        q.tile = c.tile;
-        q.stages = c.stages;
-        q.cap = c.cap;
-        q.samples = c.samples;
-        q.gate_fill = c.gate_fill;
-        const int grid = batch < units ? batch : units;
-        const cudaError_t e = launch_select(q, c.cluster, c.threads, grid, c.smem, st);
-        if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
-    }
+    // The single-block kernel goes first: at small batch it usually has no
+    // rows and ends as soon as the plan does, and the cluster kernel, placed
+    // on the GPU meanwhile (programmatic launch), starts right after it.
     {
         const PathConfig c = path_config(1, k, batch, max_seq_len, t);
         int units = 0;
@@ -296,6 +287,31 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         const int grid = (batch + per_unit - 1) / per_unit;
         const cudaError_t e = launch_select(q, 1, c.threads, grid, c.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "select launch");
+    }
+    if (launch_long) {
+        int cluster = t.cluster_size;
+        if (cluster == 0) {
+            // Blocks per long row: 16 when the long rows of the batch take at
+            // most a quarter of the SMs that way (one or two rows: the fewest
+            // bytes per SM for a latency-bound call), else 8 (16-block clusters
+            // of many rows ran slower than 8-block ones).
+            cluster = static_cast<int64_t>(batch) * 16 * 4 <= sm_count() ? 16 : 8;
+        }
+        const PathConfig c = path_config(cluster, k, batch, max_seq_len, t);
+        int units = 0;
+        const topk_status_t r = resident_units(c.cluster, c.threads, c.smem, &units);
+        if (r != TOPK_OK) return r;
+        SelectParams q = p;
+        q.items = plan_long_list(workspace);
+        q.n_items_dev = &hdr->n_long;
+        q.tile = c.tile;
+        q.stages = c.stages;
+        q.cap = c.cap;
+        q.samples = c.samples;
+        q.gate_fill = c.gate_fill;
+        const int grid = batch < units ? batch : units;
+        const cudaError_t e = launch_select(q, c.cluster, c.threads, grid, c.smem, st);
+        if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
     }
     return TOPK_OK;
 }

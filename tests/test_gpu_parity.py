@@ -74,11 +74,12 @@ def test_random_ragged_single_block(dist, k):
     compare(wl, out, raw)
 
 
+@pytest.mark.parametrize("batch", [3, 40])  # few rows: 512-thread blocks, 32 KB copies; many: 256, 16 KB
 @pytest.mark.parametrize("cluster", [2, 4, 8, 16])
 @pytest.mark.parametrize("dist", ["normal", "bf16", "flat", "neginf"])
-def test_cluster_path_forced(cluster, dist):
-    wl = workloads.random_case(seed=100 + cluster, batch=12, min_len=1, max_len=70001, k=700, page_size=16,
-                               dist=dist)
+def test_cluster_path_forced(cluster, dist, batch):
+    wl = workloads.random_case(seed=100 + cluster + batch, batch=batch, min_len=1, max_len=70001, k=700,
+                               page_size=16, dist=dist)
     with tuning(long_threshold=0, long_threshold_small_batch=0, cluster_size=cluster):
         out, raw, _ = run_gpu(wl)
     compare(wl, out, raw)

@@ -83,8 +83,13 @@ def test_plan_lists_match_oracle_classification():
 
     lib = _lib()
     rng = np.random.default_rng(1)
-    for batch, max_len in ((5, 1 << 20), (200, 300000), (8192, 8192)):
+    cases = [(5, 1 << 20, None), (200, 300000, None), (8192, 8192, None),
+             # every row in one (class, bucket): the plan writes no lists and sets the identity flag
+             (8192, 8192, 8192), (3, 1 << 20, 1 << 20), (16384, 70000, 65000), (16385, 8192, 8192)]
+    for batch, max_len, same in cases:
         lens = rng.integers(-5, max_len + 1000, size=batch).astype(np.int32)
+        if same is not None:
+            lens[:] = same
         dev = torch.device("cuda", 0)
         seq = torch.from_numpy(lens).to(dev)
         nbytes = lib.topk_plan_workspace_bytes(batch)
@@ -99,6 +104,11 @@ def test_plan_lists_match_oracle_classification():
         n_long, n_short = int(hdr[4]), int(hdr[5])
         lists = host[64:64 + 8 * batch].view(np.int32)
         long_rows, short_rows = lists[:n_long], lists[batch:batch + n_short]
+        # identity: one sweep (batch <= 16384) with a single (class, bucket)
+        assert int(hdr[7]) == int(same is not None and batch <= 16384)
+        if int(hdr[7]):
+            assert (lists == 0).all()  # nothing written
+            long_rows, short_rows = np.arange(n_long), np.arange(n_short)
         assert sorted(long_rows.tolist()) == np.nonzero(is_long)[0].tolist()
         assert sorted(short_rows.tolist()) == np.nonzero(~is_long)[0].tolist()
         assert int(hdr[6]) == flags
