@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 ptx::sts_u32(CTL(s, nemit), 0);
                 ptx::sts_u32(CTL(s, nfin), 0);
                 ptx::sts_u32(CTL(s, smax), 0);
-            }
+                    }
             __syncthreads();
 
             // ------------------------------------------------------ 1. gate
@@ -1087,27 +1087,48 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 }
             } else {
                 // ---- <= 32 candidates in [r_lo, r_hi]: warp compare-and-swap finish
+                // One pass over the buffer: entries above the range are emitted,
+                // entries inside it go to the finish list (of rank 0 in a cluster).
                 const uint32_t nc = ptx::lds_u32(CTL(s, ncand));
-                emit_from_buffer(nc, [&](uint32_t key) { return key > r_hi; });
-                for (uint32_t i = tid; i < nc; i += NT) {
-                    const uint32_t key = ptx::lds_u32(s.cand_key + 4u * i);
-                    if (key >= r_lo && key <= r_hi) {
-                        const uint32_t pos = ptx::lds_u32(s.cand_idx + 4u * i);
-                        if (C > 1) {
-                            const uint32_t slot = ptx::atom_add_cluster_u32(ptx::map_rank(CTL(s, nfin), 0), 1u);
-                            if (slot < static_cast<uint32_t>(kFinish)) {
-                                ptx::st_cluster_u32(ptx::map_rank(s.fin_key + slot * 4u, 0), key);
-                                ptx::st_cluster_u32(ptx::map_rank(s.fin_idx + slot * 4u, 0), pos);
-                            } else {
+                for (uint32_t i0 = 0; i0 < nc; i0 += 4u * NT) {
+                    uint32_t key[4], pos[4];
+                    uint32_t m = 0, f = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t i = i0 + q * NT + tid;
+                        const bool in = i < nc;
+                        key[q] = in ? ptx::lds_u32(s.cand_key + 4u * i) : 0u;
+                        pos[q] = in ? ptx::lds_u32(s.cand_idx + 4u * i) : 0u;
+                        if (in && key[q] > r_hi) m |= 1u << q;
+                        if (in && key[q] >= r_lo && key[q] <= r_hi) f |= 1u << q;
+                    }
+                    uint32_t slot = warp_reserve_n(CTL(s, nemit), __popc(m), lane);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (m >> q & 1u) {
+                            if (slot < K)
+                                ptx::sts_u32(s.emit + 4u * slot, pos[q]);
+                            else
                                 set_err(TOPK_FLAG_INTERNAL);
-                            }
-                        } else {
-                            const uint32_t slot = ptx::atom_add_s(CTL(s, nfin), 1u);
-                            if (slot < static_cast<uint32_t>(kFinish)) {
-                                ptx::sts_u32(s.fin_key + 4u * slot, key);
-                                ptx::sts_u32(s.fin_idx + 4u * slot, pos);
+                            ++slot;
+                        }
+                        if (f >> q & 1u) {
+                            if (C > 1) {
+                                const uint32_t fs = ptx::atom_add_cluster_u32(ptx::map_rank(CTL(s, nfin), 0), 1u);
+                                if (fs < static_cast<uint32_t>(kFinish)) {
+                                    ptx::st_cluster_u32(ptx::map_rank(s.fin_key + fs * 4u, 0), key[q]);
+                                    ptx::st_cluster_u32(ptx::map_rank(s.fin_idx + fs * 4u, 0), pos[q]);
+                                } else {
+                                    set_err(TOPK_FLAG_INTERNAL);
+                                }
                             } else {
-                                set_err(TOPK_FLAG_INTERNAL);
+                                const uint32_t fs = ptx::atom_add_s(CTL(s, nfin), 1u);
+                                if (fs < static_cast<uint32_t>(kFinish)) {
+                                    ptx::sts_u32(s.fin_key + 4u * fs, key[q]);
+                                    ptx::sts_u32(s.fin_idx + 4u * fs, pos[q]);
+                                } else {
+                                    set_err(TOPK_FLAG_INTERNAL);
+                                }
                             }
                         }
                     }
