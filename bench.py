@@ -253,8 +253,8 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         flush.fill_(1.0)
         step()
     torch.cuda.synchronize(dev)
-    n_long_launch = 1 if wl.max_seq_len > _threshold(wl.batch) else 0
-    launches_per_step = 2 + n_long_launch  # plan + short-row select (+ long-row cluster select)
+    # the plan + the select kernel(s) topk_transform enqueues for this shape
+    launches_per_step = 1 + _lib.topk_transform_launches(wl.batch, wl.max_seq_len, wl.k)
 
     # A step (plan + transform) is replayed from one CUDA graph, as a serving
     # loop would run it: host launch latency stays out of the timed region and
@@ -319,13 +319,6 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
            "clocks": sampler.summary() if sampler else None}
     del scores, flush
     return res
-
-
-def _threshold(batch: int) -> int:
-    from sparse_attention_indexer_uint32_gb300 import _lib
-
-    t = _lib.topk_get_tuning()
-    return t.long_threshold_small_batch if batch <= t.small_batch_max else t.long_threshold
 
 
 def time_e2e(wl, steps: int, warmup: int, local: int):

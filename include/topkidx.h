@@ -95,8 +95,10 @@ topk_status_t topk_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_
  * runtime k, ragged per-row seq_lens, power-of-two page size, optional raw
  * index output).  The rows are processed by the kernels the plan assigns:
  * long rows by a cluster of thread blocks that merge their radix histograms
- * through distributed shared memory, the others by one block each; both
- * stream the row once from HBM in the common case.
+ * through distributed shared memory, the others by one block each (or, when
+ * the whole batch fits in two waves of clusters, by the cluster kernel too,
+ * after the long rows); both stream the row once from HBM in the common
+ * case.
  *
  *   scores            device float[batch][row_stride]; row b is valid in
  *                     [0, seq_lens[b]).  16-byte aligned.  Entries up to the
@@ -127,6 +129,13 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
                              int32_t max_seq_len, const int32_t* page_table, int64_t page_table_stride,
                              int32_t page_size, int32_t k, int32_t* out_indices,
                              int32_t* out_raw_indices_or_null, void* workspace, topk_stream_t stream);
+
+/*
+ * Number of kernels one topk_transform call with these arguments enqueues
+ * under the current tuning (1 or 2), or a negative topk_status_t
+ * (TOPK_EINVAL, TOPK_EDEVICE, TOPK_ECUDA).  Enqueues nothing.
+ */
+int32_t topk_transform_launches(int32_t batch, int32_t max_seq_len, int32_t k);
 
 /*
  * The gather-and-transform pass on its own (PR #26788, commit "Dynamic
@@ -215,8 +224,8 @@ typedef struct {
     int32_t long_threshold;             /* long row if seq_len > this, larger batches           */
     int32_t small_batch_max;            /* batch size up to which the small-batch threshold holds */
     int32_t cluster_size;               /* blocks per long row: 2, 4, 8 or 16; 0: automatic (16
-                                           when batch x 16 is at most a quarter of the SMs,
-                                           else 8)                                               */
+                                           when batch x 16 is at most a quarter of the SMs, 8
+                                           while every row gets a resident cluster, else 4)      */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every
                                            row takes the two-pass streaming path                  */
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */

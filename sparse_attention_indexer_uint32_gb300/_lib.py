@@ -35,6 +35,7 @@ EXPORTED = (
     "topk_plan",
     "topk_transform",
     "topk_transform_noalloc",
+    "topk_transform_launches",
     "topk_page_transform",
     "topk_key_map",
     "topk_read_flags",
@@ -85,6 +86,8 @@ def _load() -> ctypes.CDLL:
     lib.topk_transform.restype = ctypes.c_int
     lib.topk_transform_noalloc.argtypes = [p, i64, p, i32, i32, p, i64, i32, i32, p, p, p]
     lib.topk_transform_noalloc.restype = ctypes.c_int
+    lib.topk_transform_launches.argtypes = [i32, i32, i32]
+    lib.topk_transform_launches.restype = i32
     lib.topk_page_transform.argtypes = [p, i32, i32, p, i64, i32, p, p]
     lib.topk_page_transform.restype = ctypes.c_int
     lib.topk_key_map.argtypes = [p, i64, p, p]
@@ -171,6 +174,14 @@ def topk_transform_noalloc(scores: torch.Tensor, row_stride: int, seq_lens: torc
     _check("topk_transform_noalloc", _lib.topk_transform_noalloc(
         _ptr(scores), row_stride, _ptr(seq_lens), batch, max_seq_len, _ptr(page_table), page_table_stride,
         page_size, k, _ptr(out_indices), _ptr(out_raw_indices_or_null), _stream(stream, scores.device)))
+
+
+def topk_transform_launches(batch: int, max_seq_len: int, k: int) -> int:
+    """Kernels one topk_transform call with these arguments enqueues (1 or 2)."""
+    n = _lib.topk_transform_launches(batch, max_seq_len, k)
+    if n < 0:
+        raise TopkError("topk_transform_launches", n)
+    return int(n)
 
 
 def topk_page_transform(raw_indices: torch.Tensor, batch: int, k: int, page_table: torch.Tensor,

@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             // ------------------------------------------------- 2. pass 1
             const bool buffering = !p.force_two_pass;
             // The tile loop, compiled for V float4s per thread per tile (the
-            // tile and block sizes in use give V = 2, 4 or 8).
+            // tile and block sizes in use give V = 2, 4, 6 or 8).
             auto pass1 = [&](auto v_tag) {
                 constexpr int V = decltype(v_tag)::value;
                 for (uint32_t t = 0; t < ntiles; ++t) {
@@ -754,6 +754,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             if (NT == 256) {
                 if (vec_per_tile == 8u)
                     pass1(std::integral_constant<int, 8>{});
+                else if (vec_per_tile == 6u)
+                    pass1(std::integral_constant<int, 6>{});
                 else
                     pass1(std::integral_constant<int, 4>{});
             } else {

@@ -33,9 +33,8 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // Thresholds after SGLang PR #26788 (commit "Fuse the cluster/non-cluster
 // split for small batch": long rows above 32K for small batches, 64K
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
-// PR).  Blocks per long row: chosen per call (cluster_size 0): 16 for one or
-// two rows, else 8, the cluster size both the PR and the DistRadixTopK README
-// use.
+// PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
+// 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
 topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -85,21 +84,27 @@ int sm_count() {
     return sms > 0 ? sms : 1;
 }
 
-// Launch shape of the select kernel.  Bulk copies are 16 KB (32 KB when few
-// cluster rows must each pull more bytes per SM): smaller copies cost more
-// per byte.  Single blocks: a 2-stage ring and a candidate buffer of 4k
-// entries (>= 2048; >= 3072 for rows over 16K), 3 blocks per SM at k = 512
-// on rows up to 16K, 2 on longer rows.  Clusters: 3 x 16 KB (two
-// blocks per SM) when the long rows can fill the GPU, 5 x 32 KB when they
-// cannot.
+// Launch shape of the select kernel.  Larger bulk copies cost less per byte
+// (the per-copy work of a warp is amortised over more elements), within the
+// shared memory that keeps two or three blocks per SM.  Single blocks: a
+// candidate buffer of 4k entries (>= 2048; >= 3072 for rows over 16K).
+// Clusters: a k-entry buffer (>= 2048).
 PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_len, const topk_tuning_t& t) {
     PathConfig c;
     c.cluster = cluster;
     const bool few_rows = cluster > 1 && static_cast<int64_t>(batch) * cluster * 2 <= sm_count();
-    // floats per bulk copy: 32 KB for long single-block rows and for few long
-    // cluster rows, 16 KB otherwise (short rows keep 3 blocks per SM).
-    c.tile = (few_rows || (cluster == 1 && max_seq_len > 16384)) ? 8192 : 4096;
-    c.stages = cluster == 1 ? 2 : (few_rows ? 5 : 3);
+    // floats per bulk copy and ring depth: single blocks 2 x 32 KB on rows over
+    // 16K (2 x 16 KB below, three blocks per SM); clusters of few rows 5 x 32 KB
+    // (one 512-thread block per SM), else 2 x 24 KB (two 256-thread blocks per
+    // SM).  The select kernel is compiled for 2, 4, 6 or 8 float4s per thread
+    // per copy: 256 threads take 16, 24 or 32 KB copies, 512 threads 16 or 32 KB.
+    if (cluster == 1) {
+        c.tile = max_seq_len > 16384 ? 8192 : 4096;
+        c.stages = 2;
+    } else {
+        c.tile = few_rows ? 8192 : 6144;
+        c.stages = few_rows ? 5 : 2;
+    }
     // Threads per block: single blocks 256 (three blocks per SM on short
     // rows), or 512 on long rows when asked; clusters 512 when few rows pull
     // 32 KB copies, else 256 (more float4s per thread per copy).
@@ -153,6 +158,42 @@ topk_status_t resident_units(int cluster, int threads, size_t smem, int* units) 
     std::lock_guard<std::mutex> lock(g_mutex);
     cache[key] = u;
     *units = u;
+    return TOPK_OK;
+}
+
+// The kernels one topk_transform call launches.  Long rows go to the cluster
+// kernel.  Blocks per row (cluster_size 0): 16 for one or two rows, 8 while
+// every row gets a resident cluster at once, else 4.  When the whole batch
+// fits in two waves of those clusters, the short rows are handed to the
+// cluster kernel as well (after the long ones), so that no second launch runs
+// after it.
+struct Dispatch {
+    bool launch_long = false;
+    bool fold_short = false;
+    PathConfig cl = {};
+    int cl_units = 0;
+};
+
+topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, const topk_tuning_t& t, Dispatch* d) {
+    *d = Dispatch();
+    d->launch_long = max_seq_len > long_threshold(t, batch);
+    if (!d->launch_long) return TOPK_OK;
+    int cluster = t.cluster_size;
+    if (cluster == 0) {
+        if (static_cast<int64_t>(batch) * 16 * 4 <= sm_count()) {
+            cluster = 16;
+        } else {
+            const PathConfig c8 = path_config(8, k, batch, max_seq_len, t);
+            int u8 = 0;
+            const topk_status_t r = resident_units(8, c8.threads, c8.smem, &u8);
+            if (r != TOPK_OK) return r;
+            cluster = batch <= u8 ? 8 : 4;
+        }
+    }
+    d->cl = path_config(cluster, k, batch, max_seq_len, t);
+    const topk_status_t r = resident_units(d->cl.cluster, d->cl.threads, d->cl.smem, &d->cl_units);
+    if (r != TOPK_OK) return r;
+    d->fold_short = static_cast<int64_t>(batch) <= 2 * static_cast<int64_t>(d->cl_units);
     return TOPK_OK;
 }
 
@@ -238,7 +279,6 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
 
     topk_tuning_t t;
     topk_get_tuning(&t);
-    const int32_t threshold = long_threshold(t, batch);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     auto* hdr = static_cast<PlanHeader*>(workspace);
 
@@ -260,11 +300,19 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     p.disable_gate = t.disable_gate;
     p.timeout_ns = 2000000000ull;
 
-    const bool launch_long = max_seq_len > threshold;
-    // The single-block kernel goes first: at small batch it usually has no
-    // rows and ends as soon as the plan does, and the cluster kernel, placed
-    // on the GPU meanwhile (programmatic launch), starts right after it.
+    Dispatch d;
     {
+        const topk_status_t r = decide_dispatch(batch, max_seq_len, k, t, &d);
+        if (r != TOPK_OK) return r;
+    }
+    const bool launch_long = d.launch_long;
+    const bool fold_short = d.fold_short;
+    const PathConfig& cl = d.cl;
+    const int cl_units = d.cl_units;
+    if (!fold_short) {
+        // The single-block kernel goes first: at small batch it usually has no
+        // rows and ends as soon as the plan does, and a cluster kernel, placed
+        // on the GPU meanwhile (programmatic launch), starts right after it.
         const PathConfig c = path_config(1, k, batch, max_seq_len, t);
         int units = 0;
         const topk_status_t r = resident_units(1, c.threads, c.smem, &units);
@@ -289,31 +337,35 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         if (e != cudaSuccess) return cuda_fail(e, "select launch");
     }
     if (launch_long) {
-        int cluster = t.cluster_size;
-        if (cluster == 0) {
-            // Blocks per long row: 16 when the long rows of the batch take at
-            // most a quarter of the SMs that way (one or two rows: the fewest
-            // bytes per SM for a latency-bound call), else 8 (16-block clusters
-            // of many rows ran slower than 8-block ones).
-            cluster = static_cast<int64_t>(batch) * 16 * 4 <= sm_count() ? 16 : 8;
-        }
-        const PathConfig c = path_config(cluster, k, batch, max_seq_len, t);
-        int units = 0;
-        const topk_status_t r = resident_units(c.cluster, c.threads, c.smem, &units);
-        if (r != TOPK_OK) return r;
         SelectParams q = p;
         q.items = plan_long_list(workspace);
         q.n_items_dev = &hdr->n_long;
-        q.tile = c.tile;
-        q.stages = c.stages;
-        q.cap = c.cap;
-        q.samples = c.samples;
-        q.gate_fill = c.gate_fill;
-        const int grid = batch < units ? batch : units;
-        const cudaError_t e = launch_select(q, c.cluster, c.threads, grid, c.smem, st);
+        if (fold_short) {
+            q.items2 = plan_short_list(workspace, batch);
+            q.n_items2_dev = &hdr->n_short;
+        }
+        q.tile = cl.tile;
+        q.stages = cl.stages;
+        q.cap = cl.cap;
+        q.samples = cl.samples;
+        q.gate_fill = cl.gate_fill;
+        const int grid = batch < cl_units ? batch : cl_units;
+        const cudaError_t e = launch_select(q, cl.cluster, cl.threads, grid, cl.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "long-row select launch");
     }
     return TOPK_OK;
+}
+
+int32_t topk_transform_launches(int32_t batch, int32_t max_seq_len, int32_t k) {
+    if (batch < 1 || max_seq_len < 0 || k < 1 || k > kMaxK) return TOPK_EINVAL;
+    const topk_status_t dev = check_device();
+    if (dev != TOPK_OK) return dev;
+    topk_tuning_t t;
+    topk_get_tuning(&t);
+    Dispatch d;
+    const topk_status_t r = decide_dispatch(batch, max_seq_len, k, t, &d);
+    if (r != TOPK_OK) return r;
+    return (d.fold_short ? 0 : 1) + (d.launch_long ? 1 : 0);
 }
 
 topk_status_t topk_page_transform(const int32_t* raw_indices, int32_t batch, int32_t k, const int32_t* page_table,

@@ -118,5 +118,9 @@ def test_host_side_argument_checks_return_before_any_launch(lib):
     assert c.topk_page_transform(fake, 2, 4, fake, 1, 63, fake, None) == lib.TOPK_EINVAL
     assert c.topk_key_map(fake, -1, fake, None) == lib.TOPK_EINVAL
     assert c.topk_key_map(fake + 2, 8, fake, None) == lib.TOPK_EALIGN
+    # launch-count query
+    assert c.topk_transform_launches(0, 64, 8) == lib.TOPK_EINVAL
+    assert c.topk_transform_launches(4, -1, 8) == lib.TOPK_EINVAL
+    assert c.topk_transform_launches(4, 64, 2049) == lib.TOPK_EINVAL
     flags = ctypes.c_uint32(0)
     assert c.topk_read_flags(None, ctypes.byref(flags), 0, None) == lib.TOPK_EINVAL

@@ -164,3 +164,18 @@ def test_plan_mismatch_is_flagged_and_nothing_written():
     torch.cuda.synchronize()
     assert lib.topk_read_flags(ws) & lib.TOPK_FLAG_PLAN_MISMATCH
     assert (out.cpu().numpy() == -7).all()
+
+
+def test_launch_count_query_matches_the_dispatch():
+    lib = _lib()
+    t = lib.topk_get_tuning()
+    assert t.cluster_size == 0  # automatic
+    # short rows only: one single-block launch
+    assert lib.topk_transform_launches(8192, 8192, 512) == 1
+    assert lib.topk_transform_launches(2048, 65536, 512) == 1
+    # long rows of a small batch: the cluster kernel takes every row
+    assert lib.topk_transform_launches(1, 1 << 20, 2048) == 1
+    assert lib.topk_transform_launches(32, 1 << 20, 2048) == 1
+    assert lib.topk_transform_launches(128, 262144, 1024) == 1
+    # a large batch with long rows: single-block kernel for short rows, then the cluster kernel
+    assert lib.topk_transform_launches(4096, 262144, 512) == 2
