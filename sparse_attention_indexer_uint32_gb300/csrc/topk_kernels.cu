@@ -669,26 +669,23 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     // fills its reserved slot with key 0, which no later step selects.
                     const uint32_t lim = min(s1 - base_idx, tile);  // valid elements in this tile
                     uint32_t gmask = 0;
-                    if (lim == tile) {
-                        float4 x[V];
-    #pragma unroll
+                    {
+                        float4 x[V];  // this thread's float4s of the tile (a ragged tail is masked)
+#pragma unroll
                         for (int q = 0; q < V; ++q) x[q] = ptx::lds_f4(ring_st + 16u * (q * NT + tid));
-    #pragma unroll
+#pragma unroll
                         for (int q = 0; q < V; ++q)
-                            gmask |= ((x[q].x < f_lo ? 0u : 1u) | (x[q].y < f_lo ? 0u : 2u) | (x[q].z < f_lo ? 0u : 4u) |
-                                      (x[q].w < f_lo ? 0u : 8u))
+                            gmask |= ((x[q].x < f_lo ? 0u : 1u) | (x[q].y < f_lo ? 0u : 2u) |
+                                      (x[q].z < f_lo ? 0u : 4u) | (x[q].w < f_lo ? 0u : 8u))
                                      << (4 * q);
-                    } else {
-    #pragma unroll
+                    }
+                    if (lim != tile) {
+#pragma unroll
                         for (int q = 0; q < V; ++q) {
-                            const uint32_t v = q * NT + tid;
-                            const float4 x = ptx::lds_f4(ring_st + 16u * v);
-                            const uint32_t e0 = 4u * v;
-                            const uint32_t g = (x.x < f_lo ? 0u : 1u) | (x.y < f_lo ? 0u : 2u) |
-                                               (x.z < f_lo ? 0u : 4u) | (x.w < f_lo ? 0u : 8u);
+                            const uint32_t e0 = 4u * (q * NT + tid);
                             const uint32_t valid =
                                 e0 + 4u <= lim ? 15u : (e0 >= lim ? 0u : (1u << (lim - e0)) - 1u);
-                            gmask |= (g & valid) << (4 * q);
+                            gmask &= ~((15u & ~valid) << (4 * q));
                         }
                     }
                     // Gated elements: each lane writes only the positions of its gated
@@ -723,15 +720,13 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             ptx::sts_u32(s.cand_key + 4u * sl, pass ? key : 0u);
                         }
                     } else {
-                        // Runs of one bin within a lane take one atomic (a flat row
-                        // puts every element in the same bin).
+                        // Each lane counts its own gated elements (their float4s read
+                        // again, straight-line); runs of one bin take one atomic (a
+                        // flat row puts every element in the same bin).
                         uint32_t run_bin = 0u, run_n = 0u;
-                        while (gmask) {
-                            const int e = __ffs(gmask) - 1;
-                            gmask &= gmask - 1u;
-                            const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
-                            const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
-                            if (key >= lo) {
+                        auto count = [&](bool gated, float v) {
+                            const uint32_t key = score_key(v);
+                            if (gated && key >= lo) {
                                 const uint32_t bin = min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1));
                                 if (bin != run_bin && run_n) {
                                     ptx::red_add_s(s.hist_a + 4u * run_bin, run_n);
@@ -739,6 +734,16 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                                 }
                                 run_bin = bin;
                                 ++run_n;
+                            }
+                        };
+#pragma unroll
+                        for (int q = 0; q < V; ++q) {
+                            if ((gmask >> (4 * q)) & 15u) {
+                                const float4 y = ptx::lds_f4(ring_st + 16u * (q * NT + tid));
+                                count((gmask >> (4 * q)) & 1u, y.x);
+                                count((gmask >> (4 * q + 1)) & 1u, y.y);
+                                count((gmask >> (4 * q + 2)) & 1u, y.z);
+                                count((gmask >> (4 * q + 3)) & 1u, y.w);
                             }
                         }
                         if (run_n) ptx::red_add_s(s.hist_a + 4u * run_bin, run_n);
