@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 from sparse_attention_indexer_uint32_gb300 import workloads
-from tests.parity_util import compare, run_gpu, tuning
+from tests.parity_util import check_properties_all_rows, compare, run_gpu, tuning
 
 pytestmark = pytest.mark.gpu
 
@@ -36,6 +36,7 @@ def test_decode_workload_sampled_rows():
     wl = workloads.decode()
     out, raw, flags = run_gpu(wl)
     compare(wl, out, raw, rows=_sample_rows(wl.batch, 96))
+    check_properties_all_rows(wl, raw)
     assert flags == 0
 
 
@@ -43,6 +44,7 @@ def test_throughput_workload_sampled_rows():
     wl = workloads.throughput()
     out, raw, flags = run_gpu(wl)
     compare(wl, out, raw, rows=_sample_rows(wl.batch, 24))
+    check_properties_all_rows(wl, raw)
     assert flags == 0
 
 
@@ -51,6 +53,7 @@ def test_long_context_workload(batch):
     wl = workloads.long_context(batch)
     out, raw, flags = run_gpu(wl)
     compare(wl, out, raw, rows=None if batch <= 8 else _sample_rows(batch, 8))
+    check_properties_all_rows(wl, raw)
     assert flags == 0
 
 
