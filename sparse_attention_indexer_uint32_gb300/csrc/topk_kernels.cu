@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 ptx::sts_u32(CTL(s, nemit), 0);
                 ptx::sts_u32(CTL(s, nfin), 0);
                 ptx::sts_u32(CTL(s, smax), 0);
-                    }
+            }
             __syncthreads();
 
             // ------------------------------------------------------ 1. gate
