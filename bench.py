@@ -321,15 +321,22 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     return res
 
 
-def time_e2e(wl, steps: int, warmup: int, local: int):
-    """Same metric through the public API from pinned host buffers: H2D copy of
-    the step's inputs, plan + transform, D2H copy of the result, every step."""
+def time_e2e(wl, steps: int, warmup: int, local: int, chunks: int = 4, copy_streams: int = 1):
+    """Same metric through the public API from pinned host buffers: every step
+    copies the step's inputs host->device, plans and transforms, and copies the
+    result device->host.  The batch is cut into `chunks` row ranges; each
+    range's inputs go up on one of `copy_streams` copy streams, and its plan +
+    transform + result copy run on the compute stream as soon as that range
+    has landed, so copies and selection overlap.  (On GB300 the host->device
+    copy runs near 200 GB/s whatever the number of copy streams, so the step
+    is copy-bound; 4 ranges on one copy stream measured best.)"""
     import torch
 
     from sparse_attention_indexer_uint32_gb300 import _lib
 
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
+    comp = torch.cuda.current_stream(dev)
+    cstreams = [torch.cuda.Stream(dev) for _ in range(copy_streams)]
     h_scores = torch.from_numpy(wl.scores).pin_memory()
     h_seq = torch.from_numpy(wl.seq_lens).pin_memory()
     h_table = torch.from_numpy(wl.page_table).pin_memory()
@@ -338,25 +345,42 @@ def time_e2e(wl, steps: int, warmup: int, local: int):
     d_seq = torch.empty_like(h_seq, device=dev)
     d_table = torch.empty_like(h_table, device=dev)
     d_out = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev)
-    ws = torch.zeros(_lib.topk_plan_workspace_bytes(wl.batch), dtype=torch.uint8, device=dev)
+    cuts = np.linspace(0, wl.batch, min(chunks, wl.batch) + 1).astype(int)
+    ranges = [(int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+    ws = [torch.zeros(_lib.topk_plan_workspace_bytes(b - a), dtype=torch.uint8, device=dev) for a, b in ranges]
+    landed = [torch.cuda.Event() for _ in ranges]
+    freed = [torch.cuda.Event() for _ in ranges]
+    start = torch.cuda.Event()
 
     def step():
-        d_scores.copy_(h_scores, non_blocking=True)
-        d_seq.copy_(h_seq, non_blocking=True)
-        d_table.copy_(h_table, non_blocking=True)
-        _lib.topk_plan(d_seq, wl.batch, wl.max_seq_len, ws, stream)
-        _lib.topk_transform(d_scores, wl.row_stride, d_seq, wl.batch, wl.max_seq_len, d_table,
-                            wl.page_table.shape[1], wl.page_size, wl.k, d_out, None, ws, stream)
-        h_out.copy_(d_out, non_blocking=True)
+        start.record(comp)
+        for i, (a, b) in enumerate(ranges):
+            cs = cstreams[i % len(cstreams)]
+            cs.wait_event(start)
+            cs.wait_event(freed[i])  # the previous step's selection of this range is done with its inputs
+            with torch.cuda.stream(cs):
+                d_scores[a:b].copy_(h_scores[a:b], non_blocking=True)
+                d_seq[a:b].copy_(h_seq[a:b], non_blocking=True)
+                d_table[a:b].copy_(h_table[a:b], non_blocking=True)
+            landed[i].record(cs)
+        for i, (a, b) in enumerate(ranges):
+            comp.wait_event(landed[i])
+            _lib.topk_plan(d_seq[a:b], b - a, wl.max_seq_len, ws[i], comp)
+            _lib.topk_transform(d_scores[a:b], wl.row_stride, d_seq[a:b], b - a, wl.max_seq_len, d_table[a:b],
+                                wl.page_table.shape[1], wl.page_size, wl.k, d_out[a:b], None, ws[i], comp)
+            freed[i].record(comp)
+            h_out[a:b].copy_(d_out[a:b], non_blocking=True)
 
+    for i in range(len(ranges)):
+        freed[i].record(comp)
     for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(comp)
     for _ in range(steps):
         step()
-    e1.record(stream)
+    e1.record(comp)  # the compute stream waited for every range's copy
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / steps
     h2d = h_scores.numel() * 4 + h_seq.numel() * 4 + h_table.numel() * 4
