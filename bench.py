@@ -316,7 +316,7 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     flags = _lib.topk_read_flags(ws)
     res = {"total_ms": total_ms, "step_ms": step_ms, "plan_ms": plan_ms, "select_ms": sel_ms,
            "wall_s": t_wall, "flags": flags, "launches_per_step": launches_per_step,
-           "clocks": sampler.summary() if sampler else None}
+           "clocks": sampler.summary() if sampler else None, "out": out.cpu().numpy()}
     del scores, flush
     return res
 
@@ -411,6 +411,45 @@ def oracle_sample_time(wl, target_s: float = 12.0):
             "sample": f"first {n} of {wl.batch} rows of {wl.name}, {dt:.2f} s wall on {cores} threads"}
 
 
+def check_timed_rows(wl, out, count: int = 64, seed: int = 0) -> dict:
+    """Re-checks the output of the timed run on sampled rows, without the
+    oracle: positions are recovered through the inverse of the row's page
+    table, then each row must hold min(k, L) distinct in-range positions, no
+    unselected score above a selected one, and ties at the k-th score taken
+    at the smallest positions.  Raises on a failure."""
+    rng = np.random.default_rng(seed)
+    rows = sorted(set(rng.choice(wl.batch, size=min(count, wl.batch), replace=False).tolist()) | {0, wl.batch - 1})
+    P = wl.page_size
+    lp = P.bit_length() - 1
+    for b in rows:
+        L = int(min(max(int(wl.seq_lens[b]), 0), wl.max_seq_len))
+        n = min(wl.k, L)
+        o = out[b].astype(np.int64)
+        if not (o[n:] == -1).all():
+            raise AssertionError(f"row {b}: padding is not -1")
+        table = wl.page_table[b].astype(np.int64)
+        pages = -(-L // P)
+        order = np.argsort(table[:pages], kind="stable")
+        page_id = (o[:n] & 0xFFFFFFFF) >> lp
+        k_pos = np.searchsorted(table[:pages][order], page_id)
+        if n and ((k_pos >= pages).any() or (table[:pages][order][np.minimum(k_pos, pages - 1)] != page_id).any()):
+            raise AssertionError(f"row {b}: an output is not a page of the row's table")
+        raw = order[np.minimum(k_pos, pages - 1)] * P + (o[:n] & (P - 1))
+        if n and (len(np.unique(raw)) != n or raw.min() < 0 or raw.max() >= L):
+            raise AssertionError(f"row {b}: positions repeat or leave the row")
+        if 0 < n < L:
+            x = wl.scores[b, :L]
+            sel = np.zeros(L, dtype=bool)
+            sel[raw] = True
+            t = x[sel].min()
+            if x[~sel].max() > t:
+                raise AssertionError(f"row {b}: an unselected score beats a selected one")
+            tied = np.nonzero(x == t)[0]
+            if sel[tied].any() and (~sel[tied]).any() and tied[sel[tied]].max() > tied[~sel[tied]].min():
+                raise AssertionError(f"row {b}: ties at the k-th score not taken smallest position first")
+    return {"rows": len(rows), "result": "ok", "how": "page-table inverse + order properties, no oracle"}
+
+
 def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: int, full: bool):
     log("workload", name)
     wl = build_workload(name, shard=rank)
@@ -430,6 +469,8 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
         "dtype": "f32 scores, u32 keys, i32 indices", "data": "synthetic (seeded)",
         "config": config_of(wl, name, world),
         "us_per_call": round(ms_step * 1e3, 2),
+        "step_us_p10_p50_p90": [round(float(np.percentile(r["step_ms"], q)) * 1e3, 2) for q in (10, 50, 90)],
+        "timed_output_check": check_timed_rows(wl, r["out"]),
         "plan_us": round(statistics.mean(r["plan_ms"]) * 1e3, 2),
         "select_us": round(sel_avg * 1e3, 2),
         "algorithmic_bytes_per_step": nbytes,

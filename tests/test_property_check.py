@@ -79,3 +79,23 @@ def test_rejects_a_repeated_position_and_one_past_the_row():
     raw[b, 0] = int(min(wl.seq_lens[b], wl.max_seq_len))
     with pytest.raises(AssertionError):
         check_properties_all_rows(wl, raw)
+
+
+def test_bench_timed_output_check_accepts_the_oracle_and_rejects_a_swap():
+    import bench
+
+    for dist in ("normal", "int"):
+        wl = workloads.random_case(seed=9300 + len(dist), batch=20, min_len=0, max_len=4000, k=200, page_size=16,
+                                   dist=dist)
+        out, raw, _ = oracle.topk_transform(wl.scores, wl.seq_lens, wl.page_table, wl.page_size, wl.k,
+                                            max_seq_len=wl.max_seq_len, want_raw=True)
+        assert bench.check_timed_rows(wl, out, count=20)["result"] == "ok"
+    b = _long_row(wl)
+    L = int(min(wl.seq_lens[b], wl.max_seq_len))
+    chosen = set(raw[b, :wl.k].tolist())
+    worst = min((i for i in range(L) if i not in chosen), key=lambda i: wl.scores[b, i])
+    bad_raw = raw.copy()
+    bad_raw[b, 0] = worst
+    bad_out = oracle.page_transform(bad_raw, wl.page_table, wl.page_size)
+    with pytest.raises(AssertionError):
+        bench.check_timed_rows(wl, bad_out, count=20)
