@@ -254,3 +254,27 @@ def test_repeat_runs_identical_sets():
         assert (np.sort(out, axis=1) == np.sort(ref_out, axis=1)).all()
         assert (np.sort(raw, axis=1) == np.sort(ref_raw, axis=1)).all()
     compare(wl, ref_out, ref_raw)
+
+
+def test_many_rows_several_windows_and_plan_sweeps():
+    """A batch past one plan sweep (16384 rows) and past one window of work
+    items per block (256 rows per block): short rows with ties and a ragged
+    tail, every row checked."""
+    wl = workloads.random_case(seed=480, batch=130001, min_len=0, max_len=97, k=9, page_size=4, dist="int")
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
+def test_mixed_batch_with_long_and_short_launches():
+    """A batch large enough that the single-block kernel runs first on the short
+    rows and the cluster kernel second on the long ones."""
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    wl = workloads.random_case(seed=481, batch=400, min_len=100, max_len=140000, k=256, page_size=64,
+                               dist="bf16")
+    assert _lib.topk_transform_launches(wl.batch, wl.max_seq_len, wl.k) == 2
+    out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw, rows=_sample_rows(wl.batch, 80, seed=3))
+    check_properties_all_rows(wl, raw)
+    assert flags == 0
