@@ -97,8 +97,8 @@ def profiled_traffic(workload_name: str):
 
 class ClockSampler:
     """Samples the SM clock and the clock-event (throttle) reasons during the
-    timed region: through NVML every millisecond when libnvidia-ml can be
-    loaded (reads only), else through nvidia-smi every 200 ms."""
+    timed region: through NVML every 0.2 ms when libnvidia-ml can be loaded
+    (reads only), else through nvidia-smi every 200 ms."""
 
     # NVML clocks-event reason bits (nvml.h) reported by name
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
@@ -157,7 +157,7 @@ class ClockSampler:
                 self.reasons.add(name)
 
     def _run(self):
-        period = 0.001 if self._nvml else 0.2
+        period = 0.0002 if self._nvml else 0.2
         while not self._stop.is_set():
             try:
                 self._nvml_sample() if self._nvml else self._smi_sample()
@@ -166,7 +166,7 @@ class ClockSampler:
             self._stop.wait(period)
 
     def __enter__(self):
-        self.source = "nvml, 1 ms" if self._nvml else "nvidia-smi, 200 ms"
+        self.source = "nvml, 0.2 ms" if self._nvml else "nvidia-smi, 200 ms"
         self._thread = threading.Thread(target=self._run, daemon=True)
         self._thread.start()
         return self
