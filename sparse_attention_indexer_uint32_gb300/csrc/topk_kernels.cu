@@ -1095,7 +1095,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             } else {
                 // ---- <= 32 candidates in [r_lo, r_hi]: warp compare-and-swap finish
                 // One pass over the buffer: entries above the range are emitted,
-                // entries inside it go to the finish list (of rank 0 in a cluster).
+                // entries inside it go to the finish list (of rank 0 in a cluster),
+                // or are emitted too when all of them are taken (need == count: no
+                // sort and no barrier).
+                const bool take_range = need >= cnt;
                 const uint32_t nc = ptx::lds_u32(CTL(s, ncand));
                 for (uint32_t i0 = 0; i0 < nc; i0 += 4u * NT) {
                     uint32_t key[4], pos[4];
@@ -1106,8 +1109,9 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                         const bool in = i < nc;
                         key[q] = in ? ptx::lds_u32(s.cand_key + 4u * i) : 0u;
                         pos[q] = in ? ptx::lds_u32(s.cand_idx + 4u * i) : 0u;
-                        if (in && key[q] > r_hi) m |= 1u << q;
-                        if (in && key[q] >= r_lo && key[q] <= r_hi) f |= 1u << q;
+                        const bool in_range = in && key[q] >= r_lo && key[q] <= r_hi;
+                        if ((in && key[q] > r_hi) || (take_range && in_range)) m |= 1u << q;
+                        if (!take_range && in_range) f |= 1u << q;
                     }
                     uint32_t slot = warp_reserve_n(CTL(s, nemit), __popc(m), lane);
 #pragma unroll
@@ -1140,11 +1144,13 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                         }
                     }
                 }
-                if (C > 1)
-                    ptx::cluster_sync();
-                else
-                    __syncthreads();
-                if (rank == 0 && warp == 0) {
+                if (!take_range) {
+                    if (C > 1)
+                        ptx::cluster_sync();
+                    else
+                        __syncthreads();
+                }
+                if (!take_range && rank == 0 && warp == 0) {
                     const uint32_t nf = min(ptx::lds_u32(CTL(s, nfin)), static_cast<uint32_t>(kFinish));
                     const uint64_t e =
                         lane < static_cast<int>(nf)
