@@ -156,6 +156,15 @@ class ClockSampler:
             if len(f) > 4 + i and f[4 + i] == "Active":
                 self.reasons.add(name)
 
+    def sample_now(self):
+        """One sample from the calling thread (the host enqueues a whole timed
+        loop in well under its GPU time, so samples taken right after the
+        enqueue fall inside the timed region)."""
+        try:
+            self._nvml_sample() if self._nvml else self._smi_sample()
+        except Exception:
+            pass
+
     def _run(self):
         period = 0.0002 if self._nvml else 0.2
         while not self._stop.is_set():
@@ -294,6 +303,9 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         e0.record(stream)
         g_step.replay()
         e1.record(stream)
+    if sampler:
+        while not ev[-1][1].query():  # the GPU is still in the timed steps
+            sampler.sample_now()
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall
     if sampler:
