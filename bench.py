@@ -540,7 +540,8 @@ def main():
             "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 scores, i32 indices", "data": "synthetic (seeded)",
-            "config": config_of(wl, args.workload, 1),
+            "config": {**config_of(wl, args.workload, 1), "l2": "n/a (host)",
+                       "launch": "the CPU oracle on all host threads, one bounded sample per step"},
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
                              "sample": last["sample"]},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
