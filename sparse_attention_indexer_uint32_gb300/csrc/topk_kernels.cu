@@ -306,16 +306,20 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
 // Per row:
 //  1. Gate.  Up to `samples` scores of the row are read (prefetched while the
 //     previous row is processed).  Their keys give a lower bound `lo`: the
-//     sample's r-th largest key, r = max(E + 4 sqrt(E) + 4, the rank that
-//     fills a set share of the candidate buffer), E the expected number of samples in
-//     the top k.  The bin width is chosen so that the sampled range covers
-//     about 1024 of the 2048 bins (the "linear mapping" of the DistRadixTopK
-//     README: bins spread over the range where the threshold lies, so few
-//     elements share its bin).
-//  2. Pass 1 streams the slice through the bulk-copy ring: every element with
-//     key >= lo is counted in the histogram and pushed (key, position) into a
-//     candidate buffer in shared memory.  In a cluster the histograms are
-//     merged through distributed shared memory.
+//     sample's r-th largest key (an 11-bit sample histogram, refined on the
+//     next 11 bits when its bin is crowded), r = max(E + 4 sqrt(E) + 4, the
+//     rank expected to fill a set share of the candidate buffer), E the
+//     expected number of samples in the top k.  The bin width of the row's
+//     histogram is chosen so that [lo, sample max] covers about 1024 of the
+//     2048 bins (the "linear mapping" of the DistRadixTopK README: bins spread
+//     over the range where the threshold lies, so few elements share its bin).
+//  2. Pass 1 streams the slice through the bulk-copy ring.  Each thread tests
+//     its float4s against the float of `lo` (one compare per element); each
+//     warp reserves buffer slots for its gated elements with one atomic per
+//     copy, and the gated elements are keyed exactly, counted in the
+//     histogram and pushed (key, position) into the candidate buffer in
+//     shared memory.  In a cluster the histograms are merged through
+//     distributed shared memory.
 //  3. Resolve.  Scanning the merged histogram from the top gives the bin of
 //     the k-th key; later 11-bit rounds histogram only the candidates inside
 //     that bin, until either the bin is a single key or it holds <= 32
