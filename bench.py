@@ -72,11 +72,17 @@ def measured_peak():
 
 
 def source_digest() -> str:
+    """Digest of the CUDA sources' code (comments and blank space left out, so
+    that a comment edit keeps a profile valid)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_indexer_uint32_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(name.encode() + text.encode())
     return h.hexdigest()[:16]
 
 
