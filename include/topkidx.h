@@ -224,8 +224,9 @@ typedef struct {
     int32_t long_threshold;             /* long row if seq_len > this, larger batches           */
     int32_t small_batch_max;            /* batch size up to which the small-batch threshold holds */
     int32_t cluster_size;               /* blocks per long row: 2, 4, 8 or 16; 0: automatic (16
-                                           when batch x 16 is at most a quarter of the SMs, 8
-                                           while every row gets a resident cluster, else 4)      */
+                                           when batch x 16 is at most the SM count, 8 while every
+                                           row gets a resident cluster, else 4 unless the rows are
+                                           too long for 4-block buffers, then 8)                 */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every
                                            row takes the two-pass streaming path                  */
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */

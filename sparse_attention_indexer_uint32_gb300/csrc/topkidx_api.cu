@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -162,9 +164,11 @@ topk_status_t resident_units(int cluster, int threads, size_t smem, int* units) 
 }
 
 // The kernels one topk_transform call launches.  Long rows go to the cluster
-// kernel.  Blocks per row (cluster_size 0): 16 for one or two rows, 8 while
-// every row gets a resident cluster at once, else 4.  When the whole batch
-// fits in two waves of those clusters, the short rows are handed to the
+// kernel.  Blocks per row (cluster_size 0): 16 while the rows take at most
+// one SM per block that way, 8 while every row gets a resident cluster at
+// once, else 4 (or 8 again when the sampled gate's floor would crowd a
+// 4-block cluster's candidate buffers).  When the whole batch fits in two
+// waves of those clusters, the short rows are handed to the
 // cluster kernel as well (after the long ones), so that no second launch runs
 // after it.
 struct Dispatch {
@@ -180,14 +184,27 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
     if (!d->launch_long) return TOPK_OK;
     int cluster = t.cluster_size;
     if (cluster == 0) {
-        if (static_cast<int64_t>(batch) * 16 * 4 <= sm_count()) {
+        if (static_cast<int64_t>(batch) * 16 <= sm_count()) {
             cluster = 16;
         } else {
             const PathConfig c8 = path_config(8, k, batch, max_seq_len, t);
             int u8 = 0;
             const topk_status_t r = resident_units(8, c8.threads, c8.smem, &u8);
             if (r != TOPK_OK) return r;
-            cluster = batch <= u8 ? 8 : 4;
+            cluster = 8;
+            if (batch > u8) {
+                // 4 blocks per row unless the sampled gate's floor would crowd a
+                // block's candidate buffer: the gate passes at least about
+                // r_safe / M of a row (r_safe = E + 4 sqrt(E) + 4, E = M k / L),
+                // and a buffer should hold twice a block's share of that.
+                const PathConfig c4 = path_config(4, k, batch, max_seq_len, t);
+                const double L = static_cast<double>(max_seq_len);
+                const double M = L <= 16384.0 ? std::min(1024.0, static_cast<double>(c4.samples))
+                                              : static_cast<double>(c4.samples);
+                const double E = M * std::min(static_cast<double>(k), L) / L;
+                const double floor_per_block = (E + 4.0 * std::sqrt(E) + 4.0) * L / (M * 4.0);
+                if (2.0 * floor_per_block <= static_cast<double>(c4.cap)) cluster = 4;
+            }
         }
     }
     d->cl = path_config(cluster, k, batch, max_seq_len, t);
