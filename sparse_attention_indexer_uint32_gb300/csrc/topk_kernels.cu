@@ -727,8 +727,17 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                         // Each lane counts its own gated elements (their float4s read
                         // again, straight-line); runs of one bin take one atomic (a
                         // flat row puts every element in the same bin).
-                        uint32_t run_bin = 0u, run_n = 0u;
+                        // In a cluster (rows long enough to be split), elements equal
+                        // to the gate float (key == lo, bin 0: a flat or top-tied row)
+                        // are only counted, without keying.
+                        uint32_t run_bin = 0u, run_n = 0u, n_lo = 0u;
                         auto count = [&](bool gated, float v) {
+                            if constexpr (C > 1) {
+                                if (gated && v == f_lo) {
+                                    ++n_lo;
+                                    return;
+                                }
+                            }
                             const uint32_t key = score_key(v);
                             if (gated && key >= lo) {
                                 const uint32_t bin = min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1));
@@ -751,6 +760,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             }
                         }
                         if (run_n) ptx::red_add_s(s.hist_a + 4u * run_bin, run_n);
+                        if (C > 1 && n_lo) ptx::red_add_s(s.hist_a, n_lo);
                     }
                     __syncwarp();
                     if (lane == 0) {
