@@ -18,6 +18,9 @@ constexpr int kMaxSamples = 2048;       // gate samples per row (held 2048 / thr
 constexpr int kItemsMax = 256;          // work items staged in shared memory per window
 constexpr int kMaxK = 2048;
 constexpr int kMaxCluster = 16;
+constexpr int kSlotRankMin = kBins + 1;                   // + rank: a block's smallest key in a round's range
+constexpr int kSlotRankMax = kSlotRankMin + kMaxCluster;  // + rank: its largest
+static_assert(kSlotRankMax + kMaxCluster <= kBinsX, "rank slots fit the histogram padding");
 
 // Workspace written by the plan kernel.
 constexpr uint32_t kPlanMagic = 0x544f504bu;  // "TOPK"
@@ -90,6 +93,8 @@ struct __align__(16) Control {
     uint32_t out_cursor[2];  // rank 0 of a cluster: output slots handed out, by row parity
     uint32_t out_base;       // this block's first output slot of the current row
     uint32_t pad[2];
+    uint32_t rnd_min[2], rnd_max[2], rnd_cnt[2];  // a cluster round's in-range key min/max/count, by parity
+    uint32_t pad2[2];
 };
 
 struct Layout {

@@ -587,6 +587,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 ptx::sts_u32(CTL(s, nemit), 0);
                 ptx::sts_u32(CTL(s, nfin), 0);
                 ptx::sts_u32(CTL(s, smax), 0);
+                if (C > 1) {  // both parities: the first buffered round may be an odd one
+                    ptx::sts_u32(CTL(s, rnd_min[0]), 0xffffffffu);
+                    ptx::sts_u32(CTL(s, rnd_max[0]), 0u);
+                    ptx::sts_u32(CTL(s, rnd_cnt[0]), 0u);
+                    ptx::sts_u32(CTL(s, rnd_min[1]), 0xffffffffu);
+                    ptx::sts_u32(CTL(s, rnd_max[1]), 0u);
+                    ptx::sts_u32(CTL(s, rnd_cnt[1]), 0u);
+                }
             }
             __syncthreads();
 
@@ -919,11 +927,33 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 }
                 // One more 11-bit round over [r_lo, r_hi].
                 const int sh = shift_for_span(r_hi - r_lo);
+                const uint32_t par = static_cast<uint32_t>(round) & 1u;
                 if (!stream_mode) {
                     const uint32_t nc = ptx::lds_u32(CTL(s, ncand));
+                    uint32_t kmin = 0xffffffffu, kmax = 0u, kcnt = 0u;
                     for (uint32_t i = tid; i < nc; i += NT) {
                         const uint32_t key = ptx::lds_u32(s.cand_key + 4u * i);
-                        if (key >= r_lo && key <= r_hi) ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
+                        if (key >= r_lo && key <= r_hi) {
+                            ptx::red_add_s(h_next + 4u * ((key - r_lo) >> sh), 1u);
+                            if constexpr (C > 1) {
+                                kmin = min(kmin, key);
+                                kmax = max(kmax, key);
+                                ++kcnt;
+                            }
+                        }
+                    }
+                    if constexpr (C > 1) {
+                        // The range's smallest and largest key over the cluster (each
+                        // block's pair rides in its own slots of the merged histogram):
+                        // when they are equal, the range is one key and the rounds end.
+                        kmin = __reduce_min_sync(kFull, kmin);
+                        kmax = __reduce_max_sync(kFull, kmax);
+                        kcnt = __reduce_add_sync(kFull, kcnt);
+                        if (lane == 0) {
+                            atomicMin(&s.ctl_ptr->rnd_min[par], kmin);
+                            atomicMax(&s.ctl_ptr->rnd_max[par], kmax);
+                            atomicAdd(&s.ctl_ptr->rnd_cnt[par], kcnt);
+                        }
                     }
                 } else {
                     for (uint32_t v0 = tid; v0 < nvec_slice; v0 += 4u * NT) {
@@ -959,8 +989,29 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 __syncthreads();
                 uint32_t hr = h_next;
                 if (C > 1) {
+                    if (!stream_mode && tid == 0) {
+                        ptx::sts_u32(h_next + 4u * (kSlotRankMin + rank), ptx::lds_u32(CTL(s, rnd_min[0]) + 4u * par));
+                        ptx::sts_u32(h_next + 4u * (kSlotRankMax + rank), ptx::lds_u32(CTL(s, rnd_max[0]) + 4u * par));
+                        ptx::sts_u32(CTL(s, rnd_min[0]) + 4u * (par ^ 1u), 0xffffffffu);  // the next round's fields
+                        ptx::sts_u32(CTL(s, rnd_max[0]) + 4u * (par ^ 1u), 0u);
+                        ptx::sts_u32(CTL(s, rnd_cnt[0]) + 4u * (par ^ 1u), 0u);
+                    }
                     cluster_merge<NT, C>(s, h_next, rank, tid);
                     hr = s.hist_m;
+                    if (!stream_mode) {
+                        uint32_t gmin = 0xffffffffu, gmax = 0u;
+                        for (uint32_t q = 0; q < static_cast<uint32_t>(C); ++q) {
+                            gmin = min(gmin, ptx::lds_u32(hr + 4u * (kSlotRankMin + q)));
+                            gmax = max(gmax, ptx::lds_u32(hr + 4u * (kSlotRankMax + q)));
+                        }
+                        if (gmin == gmax) {  // one key left in the range (cluster-uniform)
+                            local_cnt = ptx::lds_u32(CTL(s, rnd_cnt[0]) + 4u * par);
+                            r_lo = gmin;
+                            r_hi = gmin;
+                            clear_hist<NT>(h_next, tid);
+                            break;
+                        }
+                    }
                 }
                 sr = scan_find<NT>(s, hr, Kp - G, tid, h_next);
                 if (sr.bin >= static_cast<uint32_t>(kBins)) {  // cannot happen: the bin holds >= need
