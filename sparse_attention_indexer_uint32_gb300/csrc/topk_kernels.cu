@@ -1301,8 +1301,6 @@ __device__ __forceinline__ int length_bucket(int32_t L) {
 // that the persistent kernels hand out the longest rows first.  Lengths are
 // loaded into registers up front (no dependent load chain), and a thread's
 // run of rows with one (class, bucket) takes one atomic.
-constexpr int kPlanThreads = 1024;
-constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kPlanPerThread = 16;  // rows held in registers per thread in one sweep
 constexpr int kPlanKeys = 128;      // 2 classes x 64 length buckets
 
@@ -1324,8 +1322,15 @@ __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t max_seq_len, uin
 // the same key counted before it).  Counts are kept per warp (no contention
 // between warps) and turned into per-warp starting offsets by one block-wide
 // exclusive scan over (key descending, warp ascending).
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_lens, int32_t batch,
-                                                            int32_t max_seq_len, int32_t threshold, void* ws) {
+// PT threads (256 for batches of up to 4096 rows, 1024 above: fewer warps
+// make the block barriers of a small batch cheaper).
+template <int PT>
+__global__ void __launch_bounds__(PT) plan_kernel(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                                  int32_t threshold, void* ws) {
+    constexpr int kPlanThreads = PT;
+    constexpr int kPlanWarps = PT / 32;
+    constexpr int kLanesPerKey = kPlanWarps / 4;  // a key's kPlanWarps counters, 4 per lane
+    static_assert(kPlanWarps >= 4 && kPlanKeys * kPlanWarps == 4 * PT, "four scan entries per thread, one key");
     __shared__ uint32_t cnt[kPlanKeys][kPlanWarps];  // per-warp counts, then per-warp cursors
     __shared__ uint32_t warp_sum[kPlanWarps];
     __shared__ uint32_t flags_s;
@@ -1381,8 +1386,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
             if (run_key != 0xffffffffu && run_len) atomicAdd(&cnt[run_key][warp], run_len);
         }
         __syncthreads();
-        // Exclusive scan over entries e = 0..4095 ordered (key desc, warp asc):
-        // thread t owns entries 4t..4t+3, which share one key.
+        // Exclusive scan over entries e = 0..4 PT - 1 ordered (key desc, warp
+        // asc): thread t owns entries 4t..4t+3, which share one key.
         const uint32_t k = kPlanKeys - 1 - (4 * tid) / kPlanWarps;
         const int w0 = (4 * tid) % kPlanWarps;
         uint32_t v[4], sum = 0;
@@ -1399,12 +1404,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* seq_l
         }
         if (lane == 31) warp_sum[warp] = incl;
         {
-            // the 8 lanes that own one key hold its whole count
+            // the kLanesPerKey lanes that own one key hold its whole count
             uint32_t key_total = sum;
-            key_total += __shfl_xor_sync(kFull, key_total, 1);
-            key_total += __shfl_xor_sync(kFull, key_total, 2);
-            key_total += __shfl_xor_sync(kFull, key_total, 4);
-            if (one_sweep && (lane & 7) == 0 && key_total == static_cast<uint32_t>(batch)) uniform_s = 1;
+#pragma unroll
+            for (int o = 1; o < kLanesPerKey; o <<= 1) key_total += __shfl_xor_sync(kFull, key_total, o);
+            if (one_sweep && (lane & (kLanesPerKey - 1)) == 0 && key_total == static_cast<uint32_t>(batch))
+                uniform_s = 1;
         }
         __syncthreads();
         uint32_t pre = 0, n_long = 0;
@@ -1603,7 +1608,10 @@ cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_o
 
 cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
                         void* workspace, cudaStream_t stream) {
-    return launch_plain(plan_kernel, dim3(1), dim3(kPlanThreads), stream, seq_lens, batch, max_seq_len, long_threshold,
+    if (batch <= 256 * kPlanPerThread)
+        return launch_plain(plan_kernel<256>, dim3(1), dim3(256), stream, seq_lens, batch, max_seq_len,
+                            long_threshold, workspace);
+    return launch_plain(plan_kernel<1024>, dim3(1), dim3(1024), stream, seq_lens, batch, max_seq_len, long_threshold,
                         workspace);
 }
 
