@@ -83,7 +83,7 @@ def test_plan_lists_match_oracle_classification():
 
     lib = _lib()
     rng = np.random.default_rng(1)
-    cases = [(5, 1 << 20, None), (200, 300000, None), (8192, 8192, None),
+    cases = [(5, 1 << 20, None), (200, 300000, None), (3000, 70000, None), (8192, 8192, None),
              # every row in one (class, bucket): the plan writes no lists and sets the identity flag
              (8192, 8192, 8192), (3, 1 << 20, 1 << 20), (16384, 70000, 65000), (16385, 8192, 8192)]
     for batch, max_len, same in cases:
