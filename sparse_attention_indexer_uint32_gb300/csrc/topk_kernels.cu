@@ -1322,8 +1322,8 @@ __device__ __forceinline__ int32_t clamp_len(int32_t L, int32_t max_seq_len, uin
 // the same key counted before it).  Counts are kept per warp (no contention
 // between warps) and turned into per-warp starting offsets by one block-wide
 // exclusive scan over (key descending, warp ascending).
-// PT threads (256 for batches of up to 4096 rows, 1024 above: fewer warps
-// make the block barriers of a small batch cheaper).
+// PT threads (256 for batches of up to 4096 rows, 512 up to 8192, 1024
+// above: fewer warps make the block barriers of a small batch cheaper).
 template <int PT>
 __global__ void __launch_bounds__(PT) plan_kernel(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
                                                   int32_t threshold, void* ws) {
@@ -1610,6 +1610,9 @@ cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_
                         void* workspace, cudaStream_t stream) {
     if (batch <= 256 * kPlanPerThread)
         return launch_plain(plan_kernel<256>, dim3(1), dim3(256), stream, seq_lens, batch, max_seq_len,
+                            long_threshold, workspace);
+    if (batch <= 512 * kPlanPerThread)
+        return launch_plain(plan_kernel<512>, dim3(1), dim3(512), stream, seq_lens, batch, max_seq_len,
                             long_threshold, workspace);
     return launch_plain(plan_kernel<1024>, dim3(1), dim3(1024), stream, seq_lens, batch, max_seq_len, long_threshold,
                         workspace);
