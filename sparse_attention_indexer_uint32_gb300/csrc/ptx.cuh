@@ -141,18 +141,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ------------------------------------------------------- 1-D bulk copy (TMA)
-// Global -> this CTA's shared memory; completion is signalled on `bar` as
-// transaction bytes.  dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-        "%4;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// Same, with the destination given as a 32-bit shared-window address.
+// Global -> this CTA's shared memory (dst a 32-bit shared-window address);
+// completion is signalled on `bar` as transaction bytes.  dst, src and bytes
+// must be multiples of 16.
 __device__ __forceinline__ void bulk_copy_g2s_addr(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
                                                    uint64_t policy) {
     asm volatile(
