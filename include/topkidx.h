@@ -239,6 +239,12 @@ typedef struct {
                                            (never tighter than the sampling bound needs)         */
     int32_t single_block_threads;       /* 0: automatic; 256 or 512: threads per block of the
                                            single-block kernel on rows longer than 16K            */
+    int32_t single_block_copy_bytes;    /* 0: automatic; 8192, 16384, 24576 or 32768: bytes per bulk
+                                           copy of the single-block kernel (taken where its block
+                                           size is compiled for that copy: 256 threads all four,
+                                           512 threads 16384 and 32768)                           */
+    int32_t single_block_stages;        /* 0: automatic; 2..8: bulk copies in flight per block of
+                                           the single-block kernel (its shared-memory ring depth) */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -65,6 +65,8 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("samples", ctypes.c_int32),
         ("gate_fill_percent", ctypes.c_int32),
         ("single_block_threads", ctypes.c_int32),
+        ("single_block_copy_bytes", ctypes.c_int32),
+        ("single_block_stages", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -418,8 +418,9 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     auto set_err = [&](uint32_t f) { atomicOr(&s.ctl_ptr->err, f); };
 
     // Consumer tile sequence number (the same in every thread); tile t of the
-    // sequence lives in ring stage t % stages.
-    uint32_t cseq = 0;
+    // sequence lives in ring stage t % stages (kept as cst) and belongs to
+    // ring round t / stages (cround), whose parity its wait takes.
+    uint32_t cseq = 0, cst = 0, cround = 0;
     // Cluster rows that reached the output step, and (rank 0, thread 0) the
     // last such row's k: row e takes its output slots from rank 0's
     // out_cursor[e & 1], which rank 0 checks and clears after the next row's
@@ -475,9 +476,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         const uint32_t win_base = cseq;
         const uint32_t win_end = win_base + ptx::lds_u32(CTL(s, win_tiles));
 
-        // Issues the bulk copy of window tile `t` (global sequence number) into
-        // stage t % stages and records its round in the stage's claim word.
-        auto issue_tile = [&](uint32_t t) {
+        // Source address and byte count of window tile `t` (global sequence number).
+        auto tile_src = [&](uint32_t t, uint32_t& bytes) -> const float* {
             const uint32_t qw = t - win_base;
             int32_t lo_i = 0, hi_i = nw - 1;  // largest item whose first tile is <= qw
             while (lo_i < hi_i) {
@@ -495,30 +495,34 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             const uint32_t off = tile_in_item * tile;
             const uint32_t elems = min(tile, n4 - off);
             const int32_t prow = static_cast<int32_t>(ptx::lds_u32(s.it_row + 4u * lo_i));
-            const float* src = p.scores + static_cast<int64_t>(prow) * p.row_stride + t0 + off;
-            const uint32_t st = t % stages;
-            ptx::mbar_arrive_expect_tx(&s.full[st], elems * 4u);
-            ptx::bulk_copy_g2s_addr(s.ring + st * tile * 4u, src, elems * 4u, &s.full[st], policy);
+            bytes = elems * 4u;
+            return p.scores + static_cast<int64_t>(prow) * p.row_stride + t0 + off;
+        };
+        // Issues the bulk copy of window tile `t` into its stage st = t % stages.
+        auto issue_tile = [&](uint32_t t, uint32_t st) {
+            uint32_t bytes;
+            const float* src = tile_src(t, bytes);
+            ptx::mbar_arrive_expect_tx(&s.full[st], bytes);
+            ptx::bulk_copy_g2s_addr(s.ring + st * tile * 4u, src, bytes, &s.full[st], policy);
         };
         // Initial fill: the stages are all free at a window boundary.
         if (tid == 0) {
             for (uint32_t t = win_base; t < win_end && t < win_base + stages; ++t) {
                 ptx::sts_u32(s.claim + 4u * (t % stages), t / stages);
-                issue_tile(t);
+                issue_tile(t, t % stages);
             }
         }
         // Called by lane 0 of every warp after it released tile t: the warp
         // whose release completed the stage refills it with tile t + stages
         // (one claim per stage and round), so the ring is refilled as soon as
         // the slowest warp is done, not when a designated producer gets to it.
-        auto refill_after = [&](uint32_t t) {
+        // (st, r: the stage and ring round of tile t.)
+        auto refill_after = [&](uint32_t t, uint32_t st, uint32_t r) {
             const uint32_t next = t + stages;
             if (next >= win_end) return;
-            const uint32_t st = t % stages;
-            const uint32_t r = t / stages;
             if (!ptx::mbar_test_wait(&s.empty[st], r & 1u)) return;
             if (atomicCAS(&s.claim_ptr[st], r, r + 1u) != r) return;
-            issue_tile(next);
+            issue_tile(next, st);
         };
 
         // Samples per row: 1024 for rows up to 16K, more for longer rows.
@@ -664,9 +668,9 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             auto pass1 = [&](auto v_tag) {
                 constexpr int V = decltype(v_tag)::value;
                 for (uint32_t t = 0; t < ntiles; ++t) {
-                    const uint32_t st = cseq % stages;
+                    const uint32_t st = cst;
                     const bool gave_up = (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) != 0u;
-                    if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], (cseq / stages) & 1u, p.timeout_ns))
+                    if (!gave_up && !ptx::mbar_wait_bounded(&s.full[st], cround & 1u, p.timeout_ns))
                         set_err(TOPK_FLAG_TIMEOUT);
                     const uint32_t off = t * tile;
                     const uint32_t ring_st = s.ring + st * tile * 4u;
@@ -700,11 +704,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             gmask &= ~((15u & ~valid) << (4 * q));
                         }
                     }
-                    // Gated elements: each lane writes only the positions of its gated
-                    // elements into its reserved slots; the warp then takes the
-                    // compacted slots one per lane to key them exactly, count them in
-                    // the histogram and fill in their keys.  When the buffer is full (or
-                    // not used) each lane counts its own elements instead.
+                    // Gated elements: each lane keys its own gated elements exactly
+                    // (re-read from the stage), counts them in the histogram and
+                    // writes (key, position) into its reserved slots.  When the buffer
+                    // is full (or not used) each lane counts its own elements instead.
                     const uint32_t cnt = __popc(gmask);
                     const WarpPrefix wp = warp_prefix_small(cnt, lane);
                     const uint32_t total = wp.total;
@@ -717,19 +720,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                             const int e = __ffs(gmask) - 1;
                             gmask &= gmask - 1u;
                             const uint32_t idx_in_tile = 4u * (static_cast<uint32_t>(e >> 2) * NT + tid) + (e & 3);
-                            ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
-                            ++slot;
-                        }
-                        __syncwarp();
-                        for (uint32_t i = lane; i < total; i += 32) {
-                            const uint32_t sl = wbase + i;
-                            const uint32_t idx_in_tile = ptx::lds_u32(s.cand_idx + 4u * sl) - base_idx;
                             const uint32_t key = score_key(__uint_as_float(ptx::lds_u32(ring_st + 4u * idx_in_tile)));
                             const bool pass = key >= lo;
                             if (pass)
                                 ptx::red_add_s(s.hist_a + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)),
                                                1u);
-                            ptx::sts_u32(s.cand_key + 4u * sl, pass ? key : 0u);
+                            ptx::sts_u32(s.cand_key + 4u * slot, pass ? key : 0u);
+                            ptx::sts_u32(s.cand_idx + 4u * slot, base_idx + idx_in_tile);
+                            ++slot;
                         }
                     } else {
                         // Each lane counts its own gated elements (their float4s read
@@ -773,9 +771,13 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     __syncwarp();
                     if (lane == 0) {
                         ptx::mbar_arrive(&s.empty[st]);
-                        refill_after(cseq);
+                        refill_after(cseq, st, cround);
                     }
                     ++cseq;
+                    if (++cst == stages) {
+                        cst = 0;
+                        ++cround;
+                    }
                 }
             };
             if (NT == 256) {
@@ -783,8 +785,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     pass1(std::integral_constant<int, 8>{});
                 else if (vec_per_tile == 6u)
                     pass1(std::integral_constant<int, 6>{});
-                else
+                else if (vec_per_tile == 4u)
                     pass1(std::integral_constant<int, 4>{});
+                else
+                    pass1(std::integral_constant<int, 2>{});
             } else {
                 if (vec_per_tile == 4u)
                     pass1(std::integral_constant<int, 4>{});

@@ -37,7 +37,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
 // 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
-topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -99,7 +99,7 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
     // 16K (2 x 16 KB below, three blocks per SM); clusters of few rows 5 x 32 KB
     // (one 512-thread block per SM), else 2 x 24 KB (two 256-thread blocks per
     // SM).  The select kernel is compiled for 2, 4, 6 or 8 float4s per thread
-    // per copy: 256 threads take 16, 24 or 32 KB copies, 512 threads 16 or 32 KB.
+    // per copy: 256 threads take 8, 16, 24 or 32 KB copies, 512 threads 16 or 32 KB.
     if (cluster == 1) {
         c.tile = max_seq_len > 16384 ? 8192 : 4096;
         c.stages = 2;
@@ -114,6 +114,16 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
         c.threads = (t.single_block_threads == 512 && c.tile == 8192) ? 512 : 256;
     else
         c.threads = few_rows ? 512 : 256;
+    if (cluster == 1) {
+        // Explicit single-block copy size (taken only where the kernel is
+        // compiled for it: 2, 4, 6 or 8 float4s per thread at 256 threads,
+        // 2 or 4 at 512) and ring depth.
+        const int tile = t.single_block_copy_bytes / 4;
+        const int v = tile / (4 * c.threads);
+        if (tile > 0 && v * 4 * c.threads == tile && (v == 2 || v == 4 || (c.threads == 256 && (v == 6 || v == 8))))
+            c.tile = tile;
+        if (t.single_block_stages > 0) c.stages = t.single_block_stages;
+    }
     int cap = t.candidate_capacity;
     if (cap == 0) {
         cap = cluster == 1 ? 4 * k : k;
@@ -255,6 +265,11 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (t->gate_fill_percent < 0 || t->gate_fill_percent > 100) return TOPK_EINVAL;
     if (t->single_block_threads != 0 && t->single_block_threads != 256 && t->single_block_threads != 512)
         return TOPK_EINVAL;
+    if (t->single_block_copy_bytes != 0 && t->single_block_copy_bytes != 8192 &&
+        t->single_block_copy_bytes != 16384 && t->single_block_copy_bytes != 24576 &&
+        t->single_block_copy_bytes != 32768)
+        return TOPK_EINVAL;
+    if (t->single_block_stages != 0 && (t->single_block_stages < 2 || t->single_block_stages > 8)) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;

@@ -69,7 +69,8 @@ def test_tuning_roundtrip_and_validation(lib):
         assert lib.topk_get_tuning().cluster_size == 4
         for field, bad in (("cluster_size", 3), ("candidate_capacity", 100), ("samples", 33),
                            ("long_threshold", -1), ("gate_fill_percent", 101), ("gate_fill_percent", -1),
-                           ("single_block_threads", 128)):
+                           ("single_block_threads", 128), ("single_block_copy_bytes", 4096), ("single_block_stages", 1),
+                           ("single_block_stages", 9)):
             t2 = lib.topk_tuning_t(**old.as_dict())
             setattr(t2, field, bad)
             with pytest.raises(lib.TopkError) as e:

@@ -145,6 +145,20 @@ def test_single_block_512_threads(dist):
     compare(wl, out, raw)
 
 
+@pytest.mark.parametrize("copy_bytes,stages", [(8192, 2), (8192, 5), (16384, 4), (24576, 3)])
+def test_single_block_copy_shapes(copy_bytes, stages):
+    """Other bulk-copy sizes and ring depths of the single-block kernel (the
+    8 KB copy is the 2-float4-per-thread tile loop): rows shorter and longer
+    than one ring, a ragged tail, ties."""
+    wl = workloads.random_case(seed=490 + copy_bytes // 4096 + stages, batch=30, min_len=0, max_len=70001, k=512,
+                               page_size=64, dist="bf16")
+    with tuning(single_block_copy_bytes=copy_bytes, single_block_stages=stages, long_threshold=1 << 30,
+                long_threshold_small_batch=1 << 30):
+        out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
 def test_trend_rows_cluster():
     """Rows with a positional trend (the gate's sample must not alias)."""
     wl = workloads.long_context(batch=2, seq_len=300000)
