@@ -245,6 +245,10 @@ typedef struct {
                                            512 threads 16384 and 32768)                           */
     int32_t single_block_stages;        /* 0: automatic; 2..8: bulk copies in flight per block of
                                            the single-block kernel (its shared-memory ring depth) */
+    int32_t gate_refresh_tiles;         /* 0: off; 1..64: the 256-thread single-block kernel
+                                           tightens a row's gate every this many bulk copies from
+                                           the counts of its histogram so far (a monotone gate that
+                                           never drops a top-k element); other kernels ignore it  */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

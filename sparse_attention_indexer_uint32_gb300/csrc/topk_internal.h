@@ -75,6 +75,7 @@ struct SelectParams {
     int32_t cap;              // candidate buffer entries per block
     int32_t samples;          // gate samples per row
     float gate_fill;          // share of the candidate buffer the gate aims to fill
+    int32_t gate_refresh;     // single block, 256 threads: tighten the gate every this many copies (0: never)
     int32_t force_two_pass;
     int32_t disable_gate;
     uint64_t timeout_ns;
@@ -92,7 +93,8 @@ struct __align__(16) Control {
     uint32_t win_tiles;   // bulk-copy tiles in the current window of work items
     uint32_t out_cursor[2];  // rank 0 of a cluster: output slots handed out, by row parity
     uint32_t out_base;       // this block's first output slot of the current row
-    uint32_t pad[2];
+    uint32_t tkey;           // gate refresh: the tightened gate key of the current row (0: none yet)
+    uint32_t pad;
     uint32_t rnd_min[2], rnd_max[2], rnd_cnt[2];  // a cluster round's in-range key min/max/count, by parity
     uint32_t pad2[2];
 };

@@ -334,8 +334,9 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
 //     padding with -1 (PR #26788, commit "Dynamic dispatch via the plan's
 //     cluster_threshold": the transform is a separate pass).
 // ============================================================================
-template <int NT, int C>
+template <int NT, int C, bool kRefresh = false>
 __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const SelectParams p) {
+    static_assert(!kRefresh || C == 1, "the gate refresh counts a whole row in one block");
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const Layout lay = make_layout(C, p.tile, p.stages, p.cap, p.k);
     const uint32_t sbase = ptx::smem_addr(smem_raw);
@@ -591,6 +592,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                 ptx::sts_u32(CTL(s, nemit), 0);
                 ptx::sts_u32(CTL(s, nfin), 0);
                 ptx::sts_u32(CTL(s, smax), 0);
+                if (kRefresh) ptx::sts_u32(CTL(s, tkey), 0);
                 if (C > 1) {  // both parities: the first buffered round may be an odd one
                     ptx::sts_u32(CTL(s, rnd_min[0]), 0xffffffffu);
                     ptx::sts_u32(CTL(s, rnd_max[0]), 0u);
@@ -684,6 +686,13 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     // histogram and buffered.  A false positive (a NaN under the gate)
                     // fills its reserved slot with key 0, which no later step selects.
                     const uint32_t lim = min(s1 - base_idx, tile);  // valid elements in this tile
+                    // The gate float of this copy: f_lo, or the tightened gate once a
+                    // refresh has raised it (read once per warp and copy).
+                    float f_gate = f_lo;
+                    if constexpr (kRefresh) {
+                        const uint32_t tk = ptx::lds_u32(CTL(s, tkey));
+                        if (tk > lo) f_gate = __uint_as_float((tk & 0x80000000u) ? (tk & 0x7fffffffu) : ~tk);
+                    }
                     uint32_t gmask = 0;
                     {
                         float4 x[V];  // this thread's float4s of the tile (a ragged tail is masked)
@@ -691,8 +700,8 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                         for (int q = 0; q < V; ++q) x[q] = ptx::lds_f4(ring_st + 16u * (q * NT + tid));
 #pragma unroll
                         for (int q = 0; q < V; ++q)
-                            gmask |= ((x[q].x < f_lo ? 0u : 1u) | (x[q].y < f_lo ? 0u : 2u) |
-                                      (x[q].z < f_lo ? 0u : 4u) | (x[q].w < f_lo ? 0u : 8u))
+                            gmask |= ((x[q].x < f_gate ? 0u : 1u) | (x[q].y < f_gate ? 0u : 2u) |
+                                      (x[q].z < f_gate ? 0u : 4u) | (x[q].w < f_gate ? 0u : 8u))
                                      << (4 * q);
                     }
                     if (lim != tile) {
@@ -772,6 +781,41 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     if (lane == 0) {
                         ptx::mbar_arrive(&s.empty[st]);
                         refill_after(cseq, st, cround);
+                    }
+                    if constexpr (kRefresh) {
+                        // Gate refresh (LiteTopk's "online bucketed gate"): every
+                        // gate_refresh copies one warp, taking turns, walks the live
+                        // histogram from the top to the lowest bin b with at least Kp
+                        // counted elements at or above it.  Those elements are real
+                        // elements of the row with keys >= lo + (b << shift), so the
+                        // row's Kp-th key is at least that: the gate may rise to it
+                        // and no top-k element is lost.  Counts still being added make
+                        // the walk undercount, which only lowers b (a looser gate).
+                        const uint32_t R = static_cast<uint32_t>(p.gate_refresh);
+                        if ((t + 1u) % R == 0u && static_cast<uint32_t>(warp) == ((t + 1u) / R) % (NT / 32u)) {
+                            const uint32_t top = static_cast<uint32_t>(kBins) - 64u * (static_cast<uint32_t>(lane) + 1u);
+                            uint32_t sum = 0;
+#pragma unroll
+                            for (int i = 0; i < 64; i += 4) {
+                                const uint4 q4 = ptx::lds_u4(s.hist_a + 4u * (top + i));
+                                sum += q4.x + q4.y + q4.z + q4.w;
+                            }
+                            const uint32_t incl = warp_inclusive_sum(sum, lane);  // lane 0 holds the top bins
+                            const uint32_t reach = __ballot_sync(kFull, incl >= Kp);
+                            if (reach != 0u && lane == __ffs(reach) - 1) {
+                                uint32_t acc = incl - sum;
+                                uint32_t b = top;
+                                for (int i = 63; i >= 0; --i) {
+                                    acc += ptx::lds_u32(s.hist_a + 4u * (top + i));
+                                    if (acc >= Kp) {
+                                        b = top + static_cast<uint32_t>(i);
+                                        break;
+                                    }
+                                }
+                                const uint64_t nk = static_cast<uint64_t>(lo) + (static_cast<uint64_t>(b) << shift);
+                                if (nk > lo && nk <= 0xffffffffull) atomicMax(&s.ctl_ptr->tkey, static_cast<uint32_t>(nk));
+                            }
+                        }
                     }
                     ++cseq;
                     if (++cst == stages) {
@@ -1486,7 +1530,7 @@ __global__ void key_map_kernel(const float* x, int64_t n, uint32_t* keys) {
 // Raises the kernel's dynamic shared-memory limit to the device's opt-in
 // maximum (and allows 16-block clusters) once per device.  The limit is only
 // a ceiling, so every launch below it stays valid whatever its size.
-template <int NT, int C>
+template <int NT, int C, bool R = false>
 cudaError_t ensure_attributes() {
     static std::atomic<uint64_t> done{0};
     int dev = 0;
@@ -1497,19 +1541,19 @@ cudaError_t ensure_attributes() {
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(select_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    e = cudaFuncSetAttribute(select_kernel<NT, C, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
     if (C > 8) {
-        e = cudaFuncSetAttribute(select_kernel<NT, C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(select_kernel<NT, C, R>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     done.fetch_or(bit, std::memory_order_release);
     return cudaSuccess;
 }
 
-template <int NT, int C>
+template <int NT, int C, bool R = false>
 cudaError_t launch_select_t(const SelectParams& p, int grid_units, size_t smem, cudaStream_t stream) {
-    cudaError_t e = ensure_attributes<NT, C>();
+    cudaError_t e = ensure_attributes<NT, C, R>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_units * C));
@@ -1531,7 +1575,7 @@ cudaError_t launch_select_t(const SelectParams& p, int grid_units, size_t smem, 
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, select_kernel<NT, C>, p);
+    return cudaLaunchKernelEx(&cfg, select_kernel<NT, C, R>, p);
 }
 
 template <int NT, int C>
@@ -1589,6 +1633,8 @@ cudaError_t occupancy_c(int threads, size_t smem, int* units_out) {
 
 cudaError_t launch_select(const SelectParams& p, int cluster, int threads, int grid_units, size_t smem,
                           cudaStream_t stream) {
+    if (cluster == 1 && threads == 256 && p.gate_refresh > 0)
+        return launch_select_t<256, 1, true>(p, grid_units, smem, stream);
     switch (cluster) {
         case 1: return launch_select_c<1>(p, threads, grid_units, smem, stream);
         case 2: return launch_select_c<2>(p, threads, grid_units, smem, stream);

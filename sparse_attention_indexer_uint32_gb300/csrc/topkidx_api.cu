@@ -37,7 +37,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
 // 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
-topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -270,6 +270,7 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
         t->single_block_copy_bytes != 32768)
         return TOPK_EINVAL;
     if (t->single_block_stages != 0 && (t->single_block_stages < 2 || t->single_block_stages > 8)) return TOPK_EINVAL;
+    if (t->gate_refresh_tiles < 0 || t->gate_refresh_tiles > 64) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -358,6 +359,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         }
         q.tile = c.tile;
         q.stages = c.stages;
+        q.gate_refresh = c.threads == 256 ? t.gate_refresh_tiles : 0;
         q.cap = c.cap;
         q.samples = c.samples;
         q.gate_fill = c.gate_fill;
@@ -378,6 +380,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         }
         q.tile = cl.tile;
         q.stages = cl.stages;
+        q.gate_refresh = 0;
         q.cap = cl.cap;
         q.samples = cl.samples;
         q.gate_fill = cl.gate_fill;

@@ -159,6 +159,35 @@ def test_single_block_copy_shapes(copy_bytes, stages):
     assert flags == 0
 
 
+@pytest.mark.parametrize("refresh", [1, 2, 5])
+@pytest.mark.parametrize("dist", ["normal", "bf16", "int", "flat", "neginf"])
+def test_gate_refresh(refresh, dist):
+    """The monotone gate refresh of the single-block kernel: the gate rises
+    during a row from its own counts; no top-k element may be lost (ragged
+    rows over several copies, ties, -inf rows, flat rows)."""
+    wl = workloads.random_case(seed=520 + refresh * 10 + DISTS.index(dist), batch=24, min_len=0, max_len=140001,
+                               k=700, page_size=16, dist=dist)
+    with tuning(gate_refresh_tiles=refresh, long_threshold=1 << 30, long_threshold_small_batch=1 << 30):
+        out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
+@pytest.mark.parametrize("mode", ["ungated", "two_pass", "small_copies"])
+def test_gate_refresh_modes(mode):
+    """The refresh from an open gate (every element counted until the counts
+    allow a gate: an online gate with no samples), with the histogram-only
+    first pass, and with 8 KB copies (many refreshes per row)."""
+    extra = {"ungated": dict(disable_gate=1), "two_pass": dict(force_two_pass=1),
+             "small_copies": dict(single_block_copy_bytes=8192)}[mode]
+    wl = workloads.random_case(seed=540 + len(mode), batch=16, min_len=2000, max_len=100001, k=512, page_size=64,
+                               dist="normal")
+    with tuning(gate_refresh_tiles=2, long_threshold=1 << 30, long_threshold_small_batch=1 << 30, **extra):
+        out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
 def test_trend_rows_cluster():
     """Rows with a positional trend (the gate's sample must not alias)."""
     wl = workloads.long_context(batch=2, seq_len=300000)
