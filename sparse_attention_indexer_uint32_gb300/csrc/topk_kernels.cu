@@ -783,7 +783,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                         refill_after(cseq, st, cround);
                     }
                     if constexpr (kRefresh) {
-                        // Gate refresh (LiteTopk's "online bucketed gate"): every
+                        // Gate refresh (SGLang PR #32094, "[DSA] Add LiteTopk fused
+                        // indexer top-k prefill path for SM100", the threshold-refresh
+                        // step of "Background: how LiteTopk replaces the dense top-k"
+                        // and the recall argument of its summary): every
                         // gate_refresh copies one warp, taking turns, walks the live
                         // histogram from the top to the lowest bin b with at least Kp
                         // counted elements at or above it.  Those elements are real
