@@ -249,6 +249,10 @@ typedef struct {
                                            tightens a row's gate every this many bulk copies from
                                            the counts of its histogram so far (a monotone gate that
                                            never drops a top-k element); other kernels ignore it  */
+    int32_t warp_rows;                  /* 0: off; 1: a batch whose rows are all at most 16384 long,
+                                           with k <= 512, goes to the warp-per-row kernel (one warp
+                                           per row; slower than the default on the 8192 x 8192
+                                           workload so far, hence off by default)                 */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

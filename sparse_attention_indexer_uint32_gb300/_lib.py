@@ -68,6 +68,7 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("single_block_copy_bytes", ctypes.c_int32),
         ("single_block_stages", ctypes.c_int32),
         ("gate_refresh_tiles", ctypes.c_int32),
+        ("warp_rows", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -16,6 +16,11 @@ constexpr int kSlotOverflow = kBins;    // merged slot: some block's candidate b
 constexpr int kFinish = 32;             // a warp-wide compare-and-swap sort finishes <= 32 candidates
 constexpr int kMaxSamples = 2048;       // gate samples per row (held 2048 / threads per thread)
 constexpr int kItemsMax = 256;          // work items staged in shared memory per window
+// The warp-per-row kernel (short rows in large batches).
+constexpr int kWarpThreads = 256;       // 8 warps per block, one row each at a time
+constexpr uint32_t kWarpCap = 1536;     // candidate buffer entries per warp
+constexpr uint32_t kWarpMaxLen = 16384; // longest row it takes (16-bit positions, 2 KB tie bitmap)
+constexpr int32_t kWarpMaxK = 512;      // largest k it takes (the buffer holds about 3k gated elements)
 constexpr int kMaxK = 2048;
 constexpr int kMaxCluster = 16;
 constexpr int kSlotRankMin = kBins + 1;                   // + rank: a block's smallest key in a round's range
@@ -157,5 +162,8 @@ cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_o
 cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
                                   int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream);
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream);
+cudaError_t launch_warp_select(const SelectParams& p, int grid, cudaStream_t stream);
+cudaError_t warp_select_occupancy(int* units_out);
+size_t warp_select_smem_bytes();
 
 }  // namespace topkidx

@@ -37,7 +37,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
 // 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
-topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -173,6 +173,32 @@ topk_status_t resident_units(int cluster, int threads, size_t smem, int* units) 
     return TOPK_OK;
 }
 
+// Resident blocks of the warp-per-row kernel on the current device.
+topk_status_t resident_warp_units(int* units) {
+    static std::map<int, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = cache.find(dev);
+        if (it != cache.end()) {
+            *units = it->second;
+            return TOPK_OK;
+        }
+    }
+    int u = 0;
+    const cudaError_t e = warp_select_occupancy(&u);
+    if (e != cudaSuccess) return cuda_fail(e, "warp select occupancy query");
+    if (u <= 0) {
+        snprintf(g_last_error, sizeof(g_last_error), "warp select kernel cannot be resident");
+        return TOPK_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    cache[dev] = u;
+    *units = u;
+    return TOPK_OK;
+}
+
 // The kernels one topk_transform call launches.  Long rows go to the cluster
 // kernel.  Blocks per row (cluster_size 0): 16 while the rows take at most
 // one SM per block that way, 8 while every row gets a resident cluster at
@@ -271,6 +297,7 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
         return TOPK_EINVAL;
     if (t->single_block_stages != 0 && (t->single_block_stages < 2 || t->single_block_stages > 8)) return TOPK_EINVAL;
     if (t->gate_refresh_tiles < 0 || t->gate_refresh_tiles > 64) return TOPK_EINVAL;
+    if (t->warp_rows != 0 && t->warp_rows != 1) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -342,6 +369,27 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     const bool fold_short = d.fold_short;
     const PathConfig& cl = d.cl;
     const int cl_units = d.cl_units;
+    // Short rows, when asked for: the warp-per-row kernel takes every row.
+    const bool warp_ok = t.warp_rows == 1 && !launch_long && !fold_short &&
+                         max_seq_len <= static_cast<int32_t>(kWarpMaxLen) && k <= kWarpMaxK;
+    if (warp_ok) {
+        int warp_units = 0;
+        {
+            const topk_status_t r = resident_warp_units(&warp_units);
+            if (r != TOPK_OK) return r;
+        }
+        SelectParams q = p;
+        q.items = plan_short_list(workspace, batch);
+        q.n_items_dev = &hdr->n_short;
+        q.items2 = plan_long_list(workspace);
+        q.n_items2_dev = &hdr->n_long;
+        q.gate_fill = t.gate_fill_percent > 0 ? 0.01f * static_cast<float>(t.gate_fill_percent) : 0.4f;
+        const int warps_per_block = kWarpThreads / 32;
+        const int grid = std::min(warp_units, (batch + warps_per_block - 1) / warps_per_block);
+        const cudaError_t e = launch_warp_select(q, grid, st);
+        if (e != cudaSuccess) return cuda_fail(e, "warp select launch");
+        return TOPK_OK;
+    }
     if (!fold_short) {
         // The single-block kernel goes first: at small batch it usually has no
         // rows and ends as soon as the plan does, and a cluster kernel, placed
