@@ -1,9 +1,8 @@
 """GPU parity of the warp-per-row kernel (short rows, k <= 512) against the
 CPU oracle: the kernel forced on small batches (`warp_rows = 1`), over the
 score distributions, k boundaries, special values, ragged tails and every
-fallback (a gate too tight or too loose, no gate, the histogram-only pass).
-The decode workload and the 130001-row batch of test_gpu_parity.py reach
-it through the automatic dispatch."""
+fallback (a gate too tight or too loose, no gate, the histogram-only pass),
+on batches with several rows per warp, and on the full decode workload."""
 from __future__ import annotations
 
 import numpy as np
@@ -130,3 +129,31 @@ def test_warp_ties_across_the_threshold():
             out, raw, flags = run_gpu(wl)
         compare(wl, out, raw)
         assert flags == 0
+
+
+@pytest.mark.parametrize("dist", ["bf16", "int"])
+def test_warp_many_rows_per_warp(dist):
+    """More rows than warps in flight (the grid is capped at the resident
+    blocks): each warp resolves several rows in turn, so every per-warp
+    structure must be clean again after each row."""
+    wl = workloads.random_case(seed=740 + DISTS.index(dist), batch=6000, min_len=0, max_len=3000, k=100,
+                               page_size=32, dist=dist)
+    with tuning(warp_rows=1):
+        out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
+
+
+def test_warp_decode_workload():
+    """The 8192 x 8192 decode workload through the warp kernel: sampled rows
+    against the oracle, every row against the selection properties."""
+    from tests.parity_util import check_properties_all_rows
+
+    wl = workloads.decode()
+    with tuning(warp_rows=1):
+        out, raw, flags = run_gpu(wl)
+    rng = np.random.default_rng(0)
+    rows = np.array(sorted(set(rng.choice(wl.batch, size=96, replace=False).tolist()) | {0, wl.batch - 1}))
+    compare(wl, out, raw, rows=rows)
+    check_properties_all_rows(wl, raw)
+    assert flags == 0
