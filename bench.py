@@ -516,6 +516,30 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
     return line
 
 
+def parse_tuning(spec: str) -> dict:
+    """'name=value,...' -> {name: int}, names checked against the library's
+    tuning struct (topk_tuning_t in include/topkidx.h)."""
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    fields = {name for name, _ in _lib.topk_tuning_t._fields_}
+    out = {}
+    for item in [x.strip() for x in spec.split(",") if x.strip()]:
+        name, sep, value = item.partition("=")
+        if not sep or name not in fields:
+            raise ValueError(f"--tuning: {item!r} is not name=value with a topk_tuning_t field name")
+        out[name] = int(value)
+    return out
+
+
+def apply_tuning(kv: dict) -> None:
+    from sparse_attention_indexer_uint32_gb300 import _lib
+
+    t = _lib.topk_get_tuning()
+    for name, value in kv.items():
+        setattr(t, name, value)
+    _lib.topk_set_tuning(t)  # the library validates the values
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -526,6 +550,9 @@ def main():
                     help="headline workload: batch 2048 x 64K, k=512, the shape the bandwidth figures are quoted on")
     ap.add_argument("--secondary", default="decode,long1,long8,long32,ragged",
                     help="comma list of extra workloads timed after the headline one ('' for none)")
+    ap.add_argument("--tuning", default="",
+                    help="comma list of name=value library tuning knobs set before timing, e.g. warp_rows=1 "
+                         "(recorded in each line's config)")
     args = ap.parse_args()
     world, rank, local = dist_env()
 
@@ -561,13 +588,20 @@ def main():
 
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    tuning_kv = parse_tuning(args.tuning)
+    if tuning_kv:
+        apply_tuning(tuning_kv)
     line = gpu_line(args.workload, args.steps, args.warmup, world, rank, local, full=True)
+    if tuning_kv:
+        line["config"]["tuning"] = tuning_kv
     extra = []
     for name in [s for s in args.secondary.split(",") if s]:
         try:
             sub = gpu_line(name, max(3, args.steps // 2), max(3, args.warmup // 2), world, rank, local, full=False)
             extra.append({k: sub[k] for k in ("config", "value", "vs_baseline", "us_per_call", "select_us", "plan_us",
                                               "roofline", "device_flags")})
+            if tuning_kv:
+                extra[-1]["config"]["tuning"] = tuning_kv
         except Exception as e:  # report, never hide
             extra.append({"workload": name, "error": repr(e)})
     line["secondary"] = extra
