@@ -4,18 +4,21 @@
 
 One step is one pass of the whole path over one batch: the plan kernel and
 the select + transform kernels (``topk_plan`` + ``topk_transform``).  The
-headline workload is decode: batch 8192 x seq_len 8192 fp32 N(0,1) scores,
-k=512, page size 64, permuted page table (268 MB of scores, larger than L2;
-L2 is also flushed between timed steps).  ``value`` is HBM GB/s over the
+headline workload is throughput: batch 2048 x seq_len 65536 fp32 scores
+(q.k dot products), k=512, page size 64, permuted page table (512 MiB of
+scores, larger than L2; L2 is also flushed between timed steps): the shape
+the pages quote their bandwidth figures on.  ``value`` is HBM GB/s over the
 algorithmic bytes (scores read + seq_lens read + indices written, the page
 table excluded as in SGLang PR #26788), timed with CUDA events on the
-launching stream.  Secondary lines time the throughput (2048 x 65536, q.k
-scores), long-context (1/8/32 x 1M, k=2048) and ragged workloads.
+launching stream.  Secondary entries time the decode (8192 x 8192),
+long-context (1/8/32 x 1M, k=2048) and ragged workloads.
 
 ``--impl reference`` times the CPU oracle (full sort per row, all host cores)
 on a bounded sample of the same workload.  Under torchrun every rank runs the
 same per-GPU workload (weak scaling: rows are independent, no collective on
-the data path); rank 0 prints the line.
+the data path); rank 0 prints the line.  ``--quick`` leaves out the
+end-to-end and CPU-baseline legs (for profiler runs); the timed region is the
+same.
 """
 from __future__ import annotations
 
@@ -40,6 +43,7 @@ from sparse_attention_indexer_uint32_gb300 import workloads  # noqa: E402
 
 METRIC = "top-k+page-transform HBM GB/s (fraction of peak); µs/call at batch 1, seq 1M"
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 7900.0  # GB300 HBM3e nominal; `frac` is against the measured copy bandwidth, `frac_of_spec` this
 L2_FLUSH_BYTES = 256 << 20
 # The pages' own figures for a workload of the same shape (another machine:
 # context for vs_baseline, not a target), in GB/s.
@@ -286,12 +290,25 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
     with torch.cuda.graph(g_sel):
         _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
                             wl.page_size, wl.k, out, raw, ws)
+    # plan -> transform -> a dependent consumer (the stand-alone page transform
+    # of the raw output, launched with programmatic serialization: it may be
+    # placed once every select block has written its output and triggered).
+    raw_c = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev)
+    out_c = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev)
+    g_chain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_chain):
+        _lib.topk_plan(seq, wl.batch, wl.max_seq_len, ws)
+        _lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, wl.page_table.shape[1],
+                            wl.page_size, wl.k, out, raw_c, ws)
+        _lib.topk_page_transform(raw_c, wl.batch, wl.k, table, wl.page_table.shape[1], wl.page_size, out_c)
     for _ in range(2):
         flush.fill_(1.0)
         g_step.replay()
         flush.fill_(1.0)
         g_plan.replay()
         g_sel.replay()
+        flush.fill_(1.0)
+        g_chain.replay()
     torch.cuda.synchronize(dev)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -327,12 +344,22 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         g_sel.replay()
         e2.record(stream)
     torch.cuda.synchronize(dev)
+    chain_ms = []
+    for e0, e1 in ev:
+        flush.fill_(1.0)
+        e0.record(stream)
+        g_chain.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    chain_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    if not (out_c.cpu() == out.cpu()).all():  # the consumer re-derives out from the raw output
+        raise AssertionError("the chained consumer's output differs from the transform's own")
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     plan_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev3]
     sel_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev3]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     flags = _lib.topk_read_flags(ws)
-    res = {"total_ms": total_ms, "step_ms": step_ms, "plan_ms": plan_ms, "select_ms": sel_ms,
+    res = {"total_ms": total_ms, "step_ms": step_ms, "plan_ms": plan_ms, "select_ms": sel_ms, "chain_ms": chain_ms,
            "wall_s": t_wall, "flags": flags, "launches_per_step": launches_per_step,
            "clocks": sampler.summary() if sampler else None, "out": out.cpu().numpy()}
     del scores, flush
@@ -468,7 +495,8 @@ def check_timed_rows(wl, out, count: int = 64, seed: int = 0) -> dict:
     return {"rows": len(rows), "result": "ok", "how": "page-table inverse + order properties, no oracle"}
 
 
-def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: int, full: bool):
+def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: int, full: bool,
+             quick: bool = False):
     log("workload", name)
     wl = build_workload(name, shard=rank)
     nbytes = wl.algorithmic_bytes()
@@ -491,15 +519,19 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
         "timed_output_check": check_timed_rows(wl, r["out"]),
         "plan_us": round(statistics.mean(r["plan_ms"]) * 1e3, 2),
         "select_us": round(sel_avg * 1e3, 2),
+        "chain_us": round(statistics.mean(r["chain_ms"]) * 1e3, 2),
+        "chain": "plan + transform (raw output too) + a consumer kernel (the stand-alone page transform of the "
+                 "raw output) launched with programmatic serialization, one graph, events around it",
         "algorithmic_bytes_per_step": nbytes,
         "gpu_launches": r["launches_per_step"] * steps,
         "device_flags": r["flags"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
+                     "frac_of_spec": round(achieved / SPEC_HBM_GBS, 4), "spec_peak": SPEC_HBM_GBS,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
                      "kernel": "select_kernel (topk_transform), events around the call"},
     }
-    if full:
+    if full and not quick:
         e2e_steps = max(3, min(steps, 10))
         ms, h2d, d2h = time_e2e(wl, e2e_steps, 2, local)
         log("e2e", f"{ms:.3f} ms/step")
@@ -509,10 +541,14 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
         line["e2e"] = {"value": round(job_gbs(nbytes, world, 1, ms), 2), "unit": "GB/s",
                        "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
                        "ms_per_step": round(ms, 4)}
-        line["clocks"] = r["clocks"]
         if rank == 0 and world == 1:
             line["cpu_baseline"] = oracle_sample_time(wl)
             log("cpu baseline", line["cpu_baseline"])
+    if full:
+        line["clocks"] = r["clocks"]
+    elif rank == 0 and world == 1 and not quick:
+        # the oracle beside every workload's GPU figure (a shorter sample)
+        line["cpu_baseline"] = oracle_sample_time(wl, target_s=3.0)
     return line
 
 
@@ -553,6 +589,8 @@ def main():
     ap.add_argument("--tuning", default="",
                     help="comma list of name=value library tuning knobs set before timing, e.g. warp_rows=1 "
                          "(recorded in each line's config)")
+    ap.add_argument("--quick", action="store_true",
+                    help="leave out the end-to-end and CPU-baseline legs (profiler runs); the timed region is unchanged")
     args = ap.parse_args()
     world, rank, local = dist_env()
 
@@ -591,15 +629,16 @@ def main():
     tuning_kv = parse_tuning(args.tuning)
     if tuning_kv:
         apply_tuning(tuning_kv)
-    line = gpu_line(args.workload, args.steps, args.warmup, world, rank, local, full=True)
+    line = gpu_line(args.workload, args.steps, args.warmup, world, rank, local, full=True, quick=args.quick)
     if tuning_kv:
         line["config"]["tuning"] = tuning_kv
     extra = []
     for name in [s for s in args.secondary.split(",") if s]:
         try:
-            sub = gpu_line(name, max(3, args.steps // 2), max(3, args.warmup // 2), world, rank, local, full=False)
+            sub = gpu_line(name, max(3, args.steps // 2), max(3, args.warmup // 2), world, rank, local, full=False,
+                           quick=args.quick)
             extra.append({k: sub[k] for k in ("config", "value", "vs_baseline", "us_per_call", "select_us", "plan_us",
-                                              "roofline", "device_flags")})
+                                              "chain_us", "roofline", "device_flags", "cpu_baseline") if k in sub})
             if tuning_kv:
                 extra[-1]["config"]["tuning"] = tuning_kv
         except Exception as e:  # report, never hide

@@ -187,7 +187,9 @@ topk_status_t topk_read_flags(void* workspace, uint32_t* flags_host, int32_t cle
  *     a caller workspace instead).
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process, so
+ *     do not call this entry point again on a device after cudaDeviceReset
+ *     on it (the reset unloads the array; use topk_plan + topk_transform).
  *   - Every call on a device shares the one array and leaves its contents in
  *     it.  Calls whose work can overlap on the GPU (two streams, or two host
  *     threads, at once) race on it: serialise them.
@@ -253,6 +255,11 @@ typedef struct {
                                            with k <= 512, goes to the warp-per-row kernel (one warp
                                            per row; slower than the default on the 8192 x 8192
                                            workload so far, hence off by default)                 */
+    int32_t wait_limit_us;              /* 0: 2 s; else 1..60000000: how long a select block waits
+                                           for one bulk copy of scores before it gives up, sets
+                                           TOPK_FLAG_TIMEOUT (the call's output is then void) and
+                                           stops issuing copies; the call still returns, and the
+                                           block waits for its copies in flight before it exits  */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -92,7 +92,11 @@ static int rank_compare(float a, float b) {
     uint32_t ua = float_bits(a), ub = float_bits(b);
     if (ua == ub) return 0;
     if (ca == 2) return ua > ub ? 1 : -1;
+#ifdef ORACLE_MUTATION_NAN_PAYLOAD
+    return ua > ub ? 1 : -1; /* planted mistake: negative NaNs ordered like positive ones */
+#else
     return ua < ub ? 1 : -1;
+#endif
 }
 
 /* qsort comparator: negative when x must come first (ranks higher). */

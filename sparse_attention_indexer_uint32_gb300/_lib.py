@@ -69,6 +69,7 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("single_block_stages", ctypes.c_int32),
         ("gate_refresh_tiles", ctypes.c_int32),
         ("warp_rows", ctypes.c_int32),
+        ("wait_limit_us", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

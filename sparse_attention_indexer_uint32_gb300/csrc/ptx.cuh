@@ -88,20 +88,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
 // Non-blocking probe: true if the phase with the given parity has completed.
-// (try_wait may suspend the thread for a while; test_wait never does.)
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -128,15 +115,24 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return done != 0;
 }
 
-// Waits for the phase with the given parity, giving up after `limit_ns`.
-// Returns false on timeout (the caller records it and carries on, so that
-// every thread still reaches every barrier of its block and cluster).
+// Waits for the phase with the given parity, giving up once `limit_ns` have
+// passed.  Returns false on timeout (the caller records it and carries on, so
+// that every thread still reaches every barrier of its block and cluster).
+// A blocking probe may sleep until the phase completes whatever its hint, so
+// a short limit (up to 100 us) is honoured by polling with the non-blocking
+// probe instead; longer limits sleep in hardware between probes.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    if (limit_ns <= 100000ull) {
+        while (true) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (global_timer_ns() - t0 >= limit_ns) return false;
+        }
+    }
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
+        if (global_timer_ns() - t0 >= limit_ns) return false;
     }
 }
 

@@ -22,6 +22,11 @@ constexpr uint32_t kWarpCap = 1536;     // candidate buffer entries per warp
 constexpr uint32_t kWarpMaxLen = 16384; // longest row it takes (16-bit positions, 2 KB tie bitmap)
 constexpr int32_t kWarpMaxK = 512;      // largest k it takes (the buffer holds about 3k gated elements)
 constexpr int kMaxK = 2048;
+// Bounded device waits: the default limit of a wait for a bulk copy, and the
+// limit of the drain that a block which gave up runs before it exits (its own
+// copies still in flight must land first, whatever the caller's limit).
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 constexpr int kMaxCluster = 16;
 constexpr int kSlotRankMin = kBins + 1;                   // + rank: a block's smallest key in a round's range
 constexpr int kSlotRankMax = kSlotRankMin + kMaxCluster;  // + rank: its largest

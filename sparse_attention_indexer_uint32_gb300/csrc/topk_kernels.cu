@@ -25,6 +25,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "keys.cuh"
 #include "ptx.cuh"
 #include "topk_internal.h"
 #include "topkidx.h"
@@ -33,20 +34,6 @@ namespace topkidx {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-
-// ----------------------------------------------------------------- key map
-// Order-preserving fp32 -> uint32 map (DistRadixTopK README, "Distributed
-// Radix Sort via NoC", second point).  -0.0 is first folded onto +0.0 so the
-// two tie; then the sign bit is flipped for non-negative values and every
-// bit is flipped for negative ones, which makes unsigned key order equal to
-// IEEE order.  NaNs keep their bits: positive NaNs land above +inf, negative
-// NaNs below -inf.
-__device__ __forceinline__ uint32_t score_key(float x) {
-    uint32_t u = __float_as_uint(x);
-    u = (u == 0x80000000u) ? 0u : u;
-    const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u;
-    return u ^ m;
-}
 
 __device__ __forceinline__ int bit_length(uint32_t x) { return 32 - __clz(x); }
 
@@ -506,8 +493,10 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             ptx::mbar_arrive_expect_tx(&s.full[st], bytes);
             ptx::bulk_copy_g2s_addr(s.ring + st * tile * 4u, src, bytes, &s.full[st], policy);
         };
-        // Initial fill: the stages are all free at a window boundary.
-        if (tid == 0) {
+        // Initial fill: the stages are all free at a window boundary.  A block
+        // whose wait gave up issues no more copies (a stage it gave up on may
+        // still be receiving its copy).
+        if (tid == 0 && (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) == 0u) {
             for (uint32_t t = win_base; t < win_end && t < win_base + stages; ++t) {
                 ptx::sts_u32(s.claim + 4u * (t % stages), t / stages);
                 issue_tile(t, t % stages);
@@ -518,10 +507,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         // (one claim per stage and round), so the ring is refilled as soon as
         // the slowest warp is done, not when a designated producer gets to it.
         // (st, r: the stage and ring round of tile t.)
+        // A warp that gave up waiting for a stage's copy records the timeout
+        // before it releases the stage, so the refill sees the flag and leaves
+        // the stage alone: at most one copy is ever in flight per stage.
         auto refill_after = [&](uint32_t t, uint32_t st, uint32_t r) {
             const uint32_t next = t + stages;
             if (next >= win_end) return;
             if (!ptx::mbar_test_wait(&s.empty[st], r & 1u)) return;
+            if (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) return;
             if (atomicCAS(&s.claim_ptr[st], r, r + 1u) != r) return;
             issue_tile(next, st);
         };
@@ -661,7 +654,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             // The float at the bottom of the gate: key(x) >= lo <=> !(x < f_lo) for
             // every non-NaN x (the inverse of the key map; lo = 0 gives a NaN,
             // so that everything passes).
-            const float f_lo = __uint_as_float((lo & 0x80000000u) ? (lo & 0x7fffffffu) : ~lo);
+            const float f_lo = key_float(lo);
 
             // ------------------------------------------------- 2. pass 1
             const bool buffering = !p.force_two_pass;
@@ -691,7 +684,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
                     float f_gate = f_lo;
                     if constexpr (kRefresh) {
                         const uint32_t tk = ptx::lds_u32(CTL(s, tkey));
-                        if (tk > lo) f_gate = __uint_as_float((tk & 0x80000000u) ? (tk & 0x7fffffffu) : ~tk);
+                        if (tk > lo) f_gate = key_float(tk);
                     }
                     uint32_t gmask = 0;
                     {
@@ -1316,11 +1309,12 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     }
 
     // Drain: every issued tile was consumed unless a wait gave up; then the
-    // last copy of each stage is waited for (bounded) before the block exits.
+    // last copy of each stage is waited for before the block exits, with the
+    // drain's own limit (not the caller's wait limit, which may be short).
     if (tid == 0 && (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT)) {
         for (uint32_t st = 0; st < stages; ++st) {
             const uint32_t r = ptx::lds_u32(s.claim + 4u * st);
-            if (r != 0xffffffffu) ptx::mbar_wait_bounded(&s.full[st], r & 1u, p.timeout_ns);
+            if (r != 0xffffffffu) ptx::mbar_wait_bounded(&s.full[st], r & 1u, kDrainLimitNs);
         }
     }
     if (C > 1) {
@@ -1334,6 +1328,14 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         const uint32_t err = ptx::lds_u32(CTL(s, err));
         if (err) atomicOr(p.flags, err);
     }
+    // Every output store of this block has been issued: a kernel launched
+    // after this one with programmatic serialization may be placed now (SGLang
+    // PR #26788, commit log: the dependents are triggered only after the full
+    // output is written).  It still waits for this grid's completion before
+    // reading the output.
+    __syncthreads();
+    __threadfence();
+    ptx::launch_dependents();
 }
 
 namespace {
@@ -1514,14 +1516,22 @@ __global__ void __launch_bounds__(PT) plan_kernel(const int32_t* seq_lens, int32
     }
 }
 
+// The stand-alone gather pass.  It is launched with programmatic stream
+// serialization, so that it can be placed while the select kernel that wrote
+// `raw` finishes (the select kernels trigger their dependents after their
+// last output store); it waits for that grid before reading anything.
 __global__ void page_transform_kernel(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
                                       int64_t pt_stride, int32_t log2_page, int32_t* out) {
+    ptx::grid_dependency_wait();
     const int64_t n = static_cast<int64_t>(batch) * k;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t b = i / k;
         out[i] = page_map(page_table + b * pt_stride, log2_page, raw[i]);
     }
+    __syncthreads();
+    __threadfence();
+    ptx::launch_dependents();
 }
 
 __global__ void key_map_kernel(const float* x, int64_t n, uint32_t* keys) {
@@ -1622,6 +1632,23 @@ cudaError_t launch_plain(void (*kern)(Args...), dim3 grid, dim3 block, cudaStrea
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// The same with programmatic stream serialization: the kernel may start
+// before the previous grid in the stream completes, and must wait for it
+// (griddepcontrol.wait) before its first global access.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int C>
 cudaError_t launch_select_c(const SelectParams& p, int threads, int grid_units, size_t smem, cudaStream_t stream) {
     return threads == 512 ? launch_select_t<512, C>(p, grid_units, smem, stream)
@@ -1675,8 +1702,8 @@ cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, 
                                   int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream) {
     const int64_t n = static_cast<int64_t>(batch) * k;
     const int blocks = static_cast<int>(min_i64((n + 255) / 256, 152 * 8));
-    return launch_plain(page_transform_kernel, dim3(blocks), dim3(256), stream, raw, batch, k, page_table, pt_stride,
-                        log2_page, out);
+    return launch_dependent(page_transform_kernel, dim3(blocks), dim3(256), stream, raw, batch, k, page_table,
+                            pt_stride, log2_page, out);
 }
 
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream) {

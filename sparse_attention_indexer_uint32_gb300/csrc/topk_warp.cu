@@ -36,6 +36,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "keys.cuh"
 #include "ptx.cuh"
 #include "topk_internal.h"
 #include "topkidx.h"
@@ -58,22 +59,6 @@ struct WarpSmem {
     uint16_t sel[kWarpMaxK];          // the selected positions of the current row, by output slot
 };
 static_assert(sizeof(WarpSmem) % 16 == 0, "per-warp regions stay 16-byte aligned");
-
-// Order-preserving fp32 -> uint32 map (DistRadixTopK README "Ultra Low
-// Latency Distributed Radix TopK Indexer Via NoC", "Distributed Radix Sort
-// via NoC", second point): -0.0 folds onto +0.0; then the sign bit flips for
-// non-negative values and every bit flips for negative ones.
-__device__ __forceinline__ uint32_t wkey(float x) {
-    uint32_t u = __float_as_uint(x);
-    u = (u == 0x80000000u) ? 0u : u;
-    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
-}
-
-// The float whose key is k: key(x) >= k <=> !(x < wfloat(k)) for every
-// non-NaN x; k == 0 gives a NaN, which lets every element through.
-__device__ __forceinline__ float wfloat(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 __device__ __forceinline__ int wbits(uint32_t x) { return 32 - __clz(x); }
 
@@ -279,10 +264,10 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        keys[4 * j] = wkey(sx[j].x);
-                        keys[4 * j + 1] = wkey(sx[j].y);
-                        keys[4 * j + 2] = wkey(sx[j].z);
-                        keys[4 * j + 3] = wkey(sx[j].w);
+                        keys[4 * j] = score_key(sx[j].x);
+                        keys[4 * j + 1] = score_key(sx[j].y);
+                        keys[4 * j + 2] = score_key(sx[j].z);
+                        keys[4 * j + 3] = score_key(sx[j].w);
                     }
                 }
                 uint32_t prefix = 0, pmask = 0, above = 0;
@@ -303,7 +288,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                 }
             }
         }
-        const float f_lo = wfloat(lo);
+        const float f_lo = key_float(lo);
 
         // ------------------------------------------------------ 2. pass 1
         uint32_t wcnt = 0, kmax = 0;
@@ -342,7 +327,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             if (nib >> c & 1u) {
-                                const uint32_t key = wkey(xs[c]);
+                                const uint32_t key = score_key(xs[c]);
                                 const bool pass = key >= lo;  // false only for a NaN under the gate
                                 if (slot < kWarpCap) {
                                     ws.key[slot] = pass ? key : 0u;
@@ -398,9 +383,11 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                 r_hi = nhi;
                 cnt = pk.count;
             }
-            // lo == 0 (no gate) with a -NaN (key 0) in the row: key-0 entries
-            // are not counted above, so such a row is re-read too.
-            if (total < Kp || cnt > 32u && r_lo != r_hi) from_buffer = false;
+            // The row is read again when the buffer's counted keys are fewer
+            // than Kp (the gate was tighter than the k-th key), or when the
+            // rounds ended with more than 32 entries still in a range of
+            // several keys.
+            if (total < Kp || (cnt > 32u && r_lo != r_hi)) from_buffer = false;
         }
         if (!from_buffer) {
             // ---- radix rounds over re-reads of the row; a collect pass fills
@@ -418,7 +405,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                         const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            const uint32_t key = wkey(xs[c]);
+                            const uint32_t key = score_key(xs[c]);
                             if (4u * v + c < L && key >= r_lo && key <= r_hi)
                                 atomicAdd(&ws.hist[(key - r_lo) >> sh], 1u);
                         }
@@ -448,7 +435,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint32_t idx = 4u * v + c;
-                        const uint32_t key = wkey(xs[c]);
+                        const uint32_t key = score_key(xs[c]);
                         const bool live = v < nvec && idx < L;
                         emit(live && key > r_hi, idx);
                         const bool keep = live && key >= r_lo && key <= r_hi;
@@ -520,7 +507,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint32_t idx = 4u * v + c;
-                        const uint32_t key = wkey(xs[c]);
+                        const uint32_t key = score_key(xs[c]);
                         const bool live = v < nvec && idx < L;
                         emit(live && key > T, idx);
                         if (live && key == T) atomicOr(&ws.ties[idx >> 5], 1u << (idx & 31u));
@@ -622,6 +609,12 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
     }
     err = __reduce_or_sync(kWFull, err);
     if (lane == 0 && err) atomicOr(p.flags, err);
+    // Every output store of the block has been issued: a kernel launched after
+    // this one with programmatic serialization may be placed now (it still
+    // waits for this grid's completion before it reads the output).
+    __syncthreads();
+    __threadfence();
+    ptx::launch_dependents();
 }
 
 }  // namespace

@@ -37,7 +37,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
 // 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
-topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -298,6 +298,7 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (t->single_block_stages != 0 && (t->single_block_stages < 2 || t->single_block_stages > 8)) return TOPK_EINVAL;
     if (t->gate_refresh_tiles < 0 || t->gate_refresh_tiles > 64) return TOPK_EINVAL;
     if (t->warp_rows != 0 && t->warp_rows != 1) return TOPK_EINVAL;
+    if (t->wait_limit_us < 0 || t->wait_limit_us > 60000000) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -358,7 +359,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     p.flags = &hdr->flags;
     p.force_two_pass = t.force_two_pass;
     p.disable_gate = t.disable_gate;
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = t.wait_limit_us > 0 ? 1000ull * static_cast<uint64_t>(t.wait_limit_us) : kDefaultWaitLimitNs;
 
     Dispatch d;
     {

@@ -67,11 +67,16 @@ def test_tuning_roundtrip_and_validation(lib):
         t.cluster_size = 4
         lib.topk_set_tuning(t)
         assert lib.topk_get_tuning().cluster_size == 4
+        assert old.wait_limit_us == 0  # default: 2 s
+        t.wait_limit_us = 1
+        lib.topk_set_tuning(t)
+        assert lib.topk_get_tuning().wait_limit_us == 1
         for field, bad in (("cluster_size", 3), ("candidate_capacity", 100), ("samples", 33),
                            ("long_threshold", -1), ("gate_fill_percent", 101), ("gate_fill_percent", -1),
                            ("single_block_threads", 128), ("single_block_copy_bytes", 4096), ("single_block_stages", 1),
                            ("single_block_stages", 9), ("gate_refresh_tiles", -1), ("gate_refresh_tiles", 65),
-                           ("warp_rows", 2), ("warp_rows", -1)):
+                           ("warp_rows", 2), ("warp_rows", -1), ("wait_limit_us", -1),
+                           ("wait_limit_us", 60000001)):
             t2 = lib.topk_tuning_t(**old.as_dict())
             setattr(t2, field, bad)
             with pytest.raises(lib.TopkError) as e:

@@ -2,9 +2,9 @@
 
 Bit-exact comparison of the selected index sets (raw and transformed), the -1
 padding and slot alignment, on seeded inputs: the five benchmark workloads at
-their full sizes (all rows where the oracle is quick, otherwise sampled rows)
-and small ragged cases that span several tiles, every dispatch path and the
-degenerate inputs.
+their full sizes and small ragged cases that span several tiles, every
+dispatch path and the degenerate inputs.  Every row of every case is
+compared.
 """
 from __future__ import annotations
 
@@ -17,14 +17,10 @@ from tests.parity_util import check_properties_all_rows, compare, run_gpu, tunin
 pytestmark = pytest.mark.gpu
 
 
-def _sample_rows(batch, count, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(batch, size=min(count, batch), replace=False).tolist())
-    rows.update({0, batch - 1})
-    return np.array(sorted(rows))
-
-
 # ----------------------------------------------------------- the five workloads
+# Every row of every workload is compared with the oracle (raw and
+# transformed, as sorted sets, with the -1 padding and the slot alignment);
+# the property check runs on every row as a second, oracle-free check.
 def test_tiny_workload():
     wl = workloads.tiny()
     out, raw, flags = run_gpu(wl)
@@ -32,27 +28,27 @@ def test_tiny_workload():
     assert flags == 0
 
 
-def test_decode_workload_sampled_rows():
+def test_decode_workload_all_rows():
     wl = workloads.decode()
     out, raw, flags = run_gpu(wl)
-    compare(wl, out, raw, rows=_sample_rows(wl.batch, 96))
+    compare(wl, out, raw)
     check_properties_all_rows(wl, raw)
     assert flags == 0
 
 
-def test_throughput_workload_sampled_rows():
+def test_throughput_workload_all_rows():
     wl = workloads.throughput()
     out, raw, flags = run_gpu(wl)
-    compare(wl, out, raw, rows=_sample_rows(wl.batch, 24))
+    compare(wl, out, raw)
     check_properties_all_rows(wl, raw)
     assert flags == 0
 
 
 @pytest.mark.parametrize("batch", [1, 8, 32])
-def test_long_context_workload(batch):
+def test_long_context_workload_all_rows(batch):
     wl = workloads.long_context(batch)
     out, raw, flags = run_gpu(wl)
-    compare(wl, out, raw, rows=None if batch <= 8 else _sample_rows(batch, 8))
+    compare(wl, out, raw)
     check_properties_all_rows(wl, raw)
     assert flags == 0
 
@@ -62,6 +58,27 @@ def test_ragged_workload_all_rows():
     out, raw, flags = run_gpu(wl)
     compare(wl, out, raw)
     assert flags == 0
+
+
+def test_golden_cases_on_the_gpu():
+    """The hand-worked cases (tests/golden/hand_worked.txt: ties, signed
+    zeros, -inf, NaN payload order, short and empty rows, clamped and negative
+    seq_lens, the 32-bit wrap of the transform) through the CUDA path, checked
+    against their hand-worked answers, not against the oracle."""
+    from tests.golden_cases import load_cases
+
+    for case in load_cases():
+        L = len(case.scores)
+        stride = max(4, -(-L // 4) * 4)
+        scores = np.full((1, stride), np.inf, np.float32)
+        scores[0, :L] = case.scores
+        wl = workloads.Workload(case.name, scores, np.array([case.seq_len], np.int32), case.table[None, :].copy(),
+                                case.page_size, case.k, case.max_seq_len, True)
+        out, raw, _ = run_gpu(wl)
+        n = case.k - case.pad
+        assert sorted(raw[0, :n].tolist()) == case.raw, case.name
+        assert sorted(out[0, :n].tolist()) == sorted(case.out), case.name
+        assert (raw[0, n:] == -1).all() and (out[0, n:] == -1).all(), case.name
 
 
 # ------------------------------------------------------------ small ragged cases
@@ -318,6 +335,6 @@ def test_mixed_batch_with_long_and_short_launches():
                                dist="bf16")
     assert _lib.topk_transform_launches(wl.batch, wl.max_seq_len, wl.k) == 2
     out, raw, flags = run_gpu(wl)
-    compare(wl, out, raw, rows=_sample_rows(wl.batch, 80, seed=3))
+    compare(wl, out, raw)
     check_properties_all_rows(wl, raw)
     assert flags == 0

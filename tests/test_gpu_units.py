@@ -179,3 +179,86 @@ def test_launch_count_query_matches_the_dispatch():
     assert lib.topk_transform_launches(128, 262144, 1024) == 1
     # a large batch with long rows: single-block kernel for short rows, then the cluster kernel
     assert lib.topk_transform_launches(4096, 262144, 512) == 2
+
+
+@pytest.mark.parametrize("path", ["single_block", "cluster"])
+def test_bounded_wait_gives_up_and_the_next_call_is_correct(path):
+    """A wait limit of 1 us is shorter than a bulk copy of scores takes, so the
+    select blocks give up waiting: the call must return, the flag word must
+    carry TOPK_FLAG_TIMEOUT, and a following call with the default limit (on
+    the same buffers, the same stream) must give the exact answer again.  The
+    expiry is the kernel's own bounded wait running out; nothing faults."""
+    import torch
+
+    from tests.parity_util import compare, run_gpu, tuning
+
+    lib = _lib()
+    if path == "cluster":
+        wl = workloads.random_case(seed=801, batch=160, min_len=150000, max_len=262144, k=512, page_size=64,
+                                   dist="normal")
+        thr, extra = 0, dict(cluster_size=4)
+    else:
+        wl = workloads.random_case(seed=800, batch=1200, min_len=40000, max_len=65536, k=512, page_size=64,
+                                   dist="normal")
+        thr, extra = 1 << 30, {}
+    # A wait runs out only when a copy takes longer than the limit after the
+    # first probe, which a memory-bound launch of this size shows many times;
+    # a few attempts keep the test independent of one launch's timing.
+    seen = 0
+    for _ in range(4):
+        with tuning(wait_limit_us=1, long_threshold=thr, long_threshold_small_batch=thr, **extra):
+            _, _, flags = run_gpu(wl)
+        seen |= flags
+        if flags & lib.TOPK_FLAG_TIMEOUT:
+            break
+    assert seen & lib.TOPK_FLAG_TIMEOUT, f"no wait gave up (flags {seen:#x})"
+    torch.cuda.synchronize()
+    with tuning(long_threshold=thr, long_threshold_small_batch=thr, **extra):
+        out, raw, flags = run_gpu(wl)
+    assert flags == 0
+    compare(wl, out, raw)
+
+
+def test_dependent_consumer_chained_after_the_transform():
+    """plan -> transform -> a consumer kernel on one stream with no host sync:
+    the consumer (the stand-alone page transform, launched with programmatic
+    stream serialization) may be placed as soon as every select block has
+    written its output and triggered, and waits for the select grid before it
+    reads raw_out.  raw_out is poisoned with -7 before every step, so a
+    consumer that read early would map -7 to -1 and fail the comparison."""
+    import torch
+
+    from sparse_attention_indexer_uint32_gb300 import api
+    from tests.parity_util import compare
+
+    lib = _lib()
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(5)
+    for dist, k in (("normal", 512), ("bf16", 2048)):
+        wl = workloads.random_case(seed=810 + k, batch=300, min_len=0, max_len=70001, k=k, page_size=64, dist=dist)
+        scores = torch.from_numpy(wl.scores).to(dev)
+        seq = torch.from_numpy(wl.seq_lens).to(dev)
+        table = torch.from_numpy(wl.page_table).to(dev)
+        pages = wl.page_table.shape[1]
+        table2_h = rng.permutation(wl.batch * pages).astype(np.int32).reshape(wl.batch, pages)
+        table2 = torch.from_numpy(table2_h).to(dev)
+        out = torch.empty((wl.batch, wl.k), dtype=torch.int32, device=dev)
+        raw = torch.empty_like(out)
+        out2 = torch.empty_like(out)
+        ws = torch.zeros(lib.topk_plan_workspace_bytes(wl.batch), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            raw.fill_(-7)
+            out2.fill_(-9)
+            api.plan(seq, wl.max_seq_len, ws)
+            lib.topk_transform(scores, wl.row_stride, seq, wl.batch, wl.max_seq_len, table, pages, wl.page_size,
+                               wl.k, out, raw, ws)
+            lib.topk_page_transform(raw, wl.batch, wl.k, table2, pages, wl.page_size, out2)
+            torch.cuda.synchronize()
+            g_raw, g_out2 = raw.cpu().numpy(), out2.cpu().numpy()
+            compare(wl, out.cpu().numpy(), g_raw)  # the select's own output against the oracle
+            assert (g_out2 == oracle.page_transform(g_raw, table2_h, wl.page_size)).all()
+            o_out2, _, _ = oracle.topk_transform(wl.scores, wl.seq_lens, table2_h, wl.page_size, wl.k)
+            valid = np.arange(wl.k)[None, :] < np.minimum(np.clip(wl.seq_lens, 0, wl.max_seq_len), wl.k)[:, None]
+            big = np.iinfo(np.int64).max
+            srt = lambda a: np.sort(np.where(valid, a.astype(np.int64), big), axis=1)  # noqa: E731
+            assert (srt(g_out2) == srt(o_out2)).all() and (g_out2[~valid] == -1).all()

@@ -58,10 +58,11 @@ def test_golden_case(case):
     assert (raw[n:] == -1).all()
     assert sorted(out[:n].tolist()) == sorted(case.out)
     assert (out[n:] == -1).all()
-    # slot alignment: out[j] is the transform of raw[j]
+    # slot alignment: out[j] is the transform of raw[j], in 32-bit wrap-around
     for j in range(n):
         r = int(raw[j])
-        assert out[j] == case.table[r // case.page_size] * case.page_size + r % case.page_size
+        v = (int(case.table[r // case.page_size]) * case.page_size + r % case.page_size) % (1 << 32)
+        assert int(out[j]) == (v - (1 << 32) if v >= (1 << 31) else v)
     if case.seq_len < 0:
         assert flags & oracle.FLAG_SEQ_NEGATIVE
     if case.seq_len > case.max_seq_len:
@@ -256,6 +257,7 @@ MUTANTS = [
     "ORACLE_MUTATION_SIGNED_ZERO",
     "ORACLE_MUTATION_PAGE_OFFSET",
     "ORACLE_MUTATION_NO_CLAMP_COUNT",
+    "ORACLE_MUTATION_NAN_PAYLOAD",
 ]
 
 

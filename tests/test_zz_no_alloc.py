@@ -5,8 +5,9 @@ allocator-managed runtime that only receives its inputs and outputs): the
 plan's work lists live in a fixed device array owned by the library.  This
 test checks it against the workspace-based topk_plan + topk_transform on two
 calls in a row with different inputs (the second call must not see the first
-call's lists), bit-exact as sorted index sets, and that a batch above the
-array's limit is refused.  The file name makes pytest collect it last.
+call's lists), bit-exact as sorted index sets, checks both calls against the
+CPU oracle as well, and checks that a batch above the array's limit is
+refused.  The file name makes pytest collect it last.
 """
 from __future__ import annotations
 
@@ -52,6 +53,8 @@ def test_no_alloc_matches_workspace_entry_point_on_two_calls():
         # a different batch and k: the second call must not reuse the first call's lists
         workloads.random_case(seed=72, batch=9, min_len=100, max_len=40000, k=2048, page_size=16, dist="normal"),
     ]
+    from tests.parity_util import compare
+
     for wl in cases:
         ref_out, ref_raw, out, raw = _run_both(wl)
         n = np.minimum(np.clip(wl.seq_lens, 0, wl.max_seq_len), wl.k)
@@ -59,6 +62,7 @@ def test_no_alloc_matches_workspace_entry_point_on_two_calls():
         assert (out[~valid] == -1).all() and (raw[~valid] == -1).all()
         assert (_sorted_valid(raw, n) == _sorted_valid(ref_raw, n)).all()
         assert (_sorted_valid(out, n) == _sorted_valid(ref_out, n)).all()
+        compare(wl, out, raw)  # and against the CPU oracle, row by row
 
 
 def test_no_alloc_refuses_a_batch_above_its_limit():
