@@ -344,14 +344,14 @@ def time_gpu(wl, steps: int, warmup: int, local: int, world: int, want_clocks: b
         g_sel.replay()
         e2.record(stream)
     torch.cuda.synchronize(dev)
-    chain_ms = []
-    for e0, e1 in ev:
+    evc = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evc:
         flush.fill_(1.0)
         e0.record(stream)
         g_chain.replay()
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    chain_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    chain_ms = [e0.elapsed_time(e1) for e0, e1 in evc]
     if not (out_c.cpu() == out.cpu()).all():  # the consumer re-derives out from the raw output
         raise AssertionError("the chained consumer's output differs from the transform's own")
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]

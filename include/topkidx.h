@@ -260,6 +260,11 @@ typedef struct {
                                            TOPK_FLAG_TIMEOUT (the call's output is then void) and
                                            stops issuing copies; the call still returns, and the
                                            block waits for its copies in flight before it exits  */
+    int32_t single_block_kernel;        /* 0: automatic (the warp-specialised kernel for rows over
+                                           16384 when two of its blocks fit on an SM, else the
+                                           single-role kernel); 1: always the single-role kernel;
+                                           2: always the warp-specialised kernel, in which 8 warps
+                                           stream row q while 4 warps finish row q - 1           */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -70,6 +70,7 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("gate_refresh_tiles", ctypes.c_int32),
         ("warp_rows", ctypes.c_int32),
         ("wait_limit_us", ctypes.c_int32),
+        ("single_block_kernel", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

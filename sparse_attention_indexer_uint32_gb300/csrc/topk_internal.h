@@ -157,6 +157,68 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
     return l;
 }
 
+// The warp-specialised single-block kernel (topk_stream.cu): 8 streaming
+// warps run pass 1 of row q while 4 resolving warps finish row q - 1 and
+// compute the gate of row q + 1, with two candidate-buffer / histogram sets.
+constexpr int kStreamWarps = 8;
+constexpr int kResolveWarps = 4;
+constexpr int kStreamThreads = 32 * (kStreamWarps + kResolveWarps);
+
+struct __align__(16) SetControl {
+    uint32_t ncand[2];  // candidates in set b (pass 1, or a collect pass)
+    uint32_t lo[2];     // gate key of the row held by set b
+    uint32_t shift[2];  // bin shift of set b's first histogram
+    uint32_t pad[2];
+};
+
+struct StreamLayout {
+    uint32_t ring, hist[2], cand_key[2], cand_idx[2], emit, fin_key, fin_idx, warp_tot, ctl, sctl;
+    uint32_t items_row, items_len, items_tiles, items_tile_start, claim, mbar, total;
+};
+
+__host__ __device__ inline StreamLayout make_stream_layout(int tile, int stages, int cap, int k) {
+    StreamLayout l;
+    uint32_t o = 0;
+    l.ring = o;
+    o = align_up(o + static_cast<uint32_t>(stages) * tile * 4u, 128);
+    for (int b = 0; b < 2; ++b) {
+        l.hist[b] = o;
+        o += kBinsX * 4u;
+    }
+    for (int b = 0; b < 2; ++b) {
+        l.cand_key[b] = o;
+        o += static_cast<uint32_t>(cap) * 4u;
+        l.cand_idx[b] = o;
+        o += static_cast<uint32_t>(cap) * 4u;
+    }
+    l.emit = o;
+    o += align_up(static_cast<uint32_t>(k), 4) * 4u;
+    l.fin_key = o;
+    o += kFinish * 4u;
+    l.fin_idx = o;
+    o += kFinish * 4u;
+    l.warp_tot = o;
+    o += 32 * 4u;
+    l.ctl = o;
+    o += align_up(sizeof(Control), 16);
+    l.sctl = o;
+    o += align_up(sizeof(SetControl), 16);
+    l.items_row = o;
+    o += kItemsMax * 4u;
+    l.items_len = o;
+    o += kItemsMax * 4u;
+    l.items_tiles = o;
+    o += kItemsMax * 4u;
+    l.items_tile_start = o;
+    o += kItemsMax * 4u;
+    l.claim = o;
+    o += align_up(static_cast<uint32_t>(stages), 4) * 4u;
+    l.mbar = align_up(o, 8);
+    o = l.mbar + (2u * stages + 4u) * 8u;  // full[stages], empty[stages], ready[2], done[2]
+    l.total = align_up(o, 128);
+    return l;
+}
+
 // Host-side launchers (defined in topk_kernels.cu).
 cudaError_t launch_plan(const int32_t* seq_lens, int32_t batch, int32_t max_seq_len, int32_t long_threshold,
                         void* workspace, cudaStream_t stream);
@@ -168,6 +230,9 @@ cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, 
                                   int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream);
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream);
 cudaError_t launch_warp_select(const SelectParams& p, int grid, cudaStream_t stream);
+// The warp-specialised single-block kernel (topk_stream.cu).
+cudaError_t launch_stream_select(const SelectParams& p, int grid, size_t smem, cudaStream_t stream);
+cudaError_t stream_select_occupancy(size_t smem, int* units_out);
 cudaError_t warp_select_occupancy(int* units_out);
 size_t warp_select_smem_bytes();
 

@@ -291,10 +291,18 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
         const float f_lo = key_float(lo);
 
         // ------------------------------------------------------ 2. pass 1
+        // Each step tests 32 floats per lane against the gate and appends the
+        // ones that pass, as raw bits with their positions, to the warp's
+        // buffer (slots from a warp prefix of the lane counts).  Keying is left
+        // to one sweep over the compacted buffer afterwards, so the per-element
+        // work here is a compare and, for the few that pass, two stores.  Only
+        // the last step of a row is masked to the row's end, and the two
+        // register buffers alternate, so the next step's loads are always in
+        // flight while a step is tested.
         uint32_t wcnt = 0, kmax = 0;
         const bool buffering = !p.force_two_pass;
         if (buffering) {
-            float4 cur[kWVec], nxt[kWVec];
+            float4 xa[kWVec], xb[kWVec];
             auto load = [&](float4* x, uint32_t step) {
 #pragma unroll
                 for (int q = 0; q < kWVec; ++q) {
@@ -302,49 +310,62 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                     x[q] = v < nvec ? __ldg(row4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             };
-            load(cur, 0u);
-            for (uint32_t step = 0; step < nsteps; ++step) {
-                if (step + 1u < nsteps) load(nxt, step + 1u);
+            auto test = [&](const float4* x, uint32_t step) {
                 uint32_t gmask = 0;
 #pragma unroll
-                for (int q = 0; q < kWVec; ++q) {
-                    const uint32_t e0 = 4u * (step * kWStep + static_cast<uint32_t>(q * 32 + lane));
-                    const uint32_t valid = e0 + 4u <= L ? 15u : (e0 >= L ? 0u : (1u << (L - e0)) - 1u);
-                    const uint32_t g = (cur[q].x < f_lo ? 0u : 1u) | (cur[q].y < f_lo ? 0u : 2u) |
-                                       (cur[q].z < f_lo ? 0u : 4u) | (cur[q].w < f_lo ? 0u : 8u);
-                    gmask |= (g & valid) << (4 * q);
+                for (int q = 0; q < kWVec; ++q)
+                    gmask |= ((x[q].x < f_lo ? 0u : 1u) | (x[q].y < f_lo ? 0u : 2u) | (x[q].z < f_lo ? 0u : 4u) |
+                              (x[q].w < f_lo ? 0u : 8u))
+                             << (4 * q);
+                if ((step + 1u) * 4u * kWStep > L) {  // the row ends inside this step
+#pragma unroll
+                    for (int q = 0; q < kWVec; ++q) {
+                        const uint32_t e0 = 4u * (step * kWStep + static_cast<uint32_t>(q * 32 + lane));
+                        const uint32_t valid = e0 + 4u <= L ? 15u : (e0 >= L ? 0u : (1u << (L - e0)) - 1u);
+                        gmask &= ~((15u & ~valid) << (4 * q));
+                    }
                 }
                 const uint32_t cnt = static_cast<uint32_t>(__popc(gmask));
                 const uint32_t incl = wsum_incl(cnt, lane);
                 uint32_t slot = wcnt + incl - cnt;
                 wcnt += __shfl_sync(kWFull, incl, 31);
+                if (__any_sync(kWFull, gmask != 0u)) {
 #pragma unroll
-                for (int q = 0; q < kWVec; ++q) {
-                    const uint32_t nib = (gmask >> (4 * q)) & 15u;
-                    if (nib) {
+                    for (int q = 0; q < kWVec; ++q) {
                         const uint32_t p0 = 4u * (step * kWStep + static_cast<uint32_t>(q * 32 + lane));
-                        const float xs[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
+                        const float xs[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            if (nib >> c & 1u) {
-                                const uint32_t key = score_key(xs[c]);
-                                const bool pass = key >= lo;  // false only for a NaN under the gate
-                                if (slot < kWarpCap) {
-                                    ws.key[slot] = pass ? key : 0u;
-                                    ws.pos[slot] = static_cast<uint16_t>(p0 + c);
-                                }
-                                if (pass) kmax = max(kmax, key);
-                                ++slot;
+                            const uint32_t t = (gmask >> (4 * q + c)) & 1u;
+                            if (t != 0u && slot < kWarpCap) {
+                                ws.key[slot] = __float_as_uint(xs[c]);
+                                ws.pos[slot] = static_cast<uint16_t>(p0 + c);
                             }
+                            slot += t;
                         }
                     }
                 }
-                if (step + 1u < nsteps) {
-#pragma unroll
-                    for (int q = 0; q < kWVec; ++q) cur[q] = nxt[q];
-                }
+            };
+            load(xa, 0u);
+            for (uint32_t step = 0; step < nsteps; step += 2u) {
+                if (step + 1u < nsteps) load(xb, step + 1u);
+                test(xa, step);
+                if (step + 2u < nsteps) load(xa, step + 2u);
+                if (step + 1u < nsteps) test(xb, step + 1u);
             }
-            kmax = __reduce_max_sync(kWFull, kmax);
+            __syncwarp();
+            if (wcnt <= kWarpCap) {
+                // Key the buffered elements.  An element that passed the float
+                // compare but whose key is below the gate can only be a NaN; it
+                // gets key 0, which no later step selects.
+                for (uint32_t i = lane; i < wcnt; i += 32u) {
+                    const uint32_t key = score_key(__uint_as_float(ws.key[i]));
+                    const uint32_t kept = key >= lo ? key : 0u;
+                    ws.key[i] = kept;
+                    kmax = max(kmax, kept);
+                }
+                kmax = __reduce_max_sync(kWFull, kmax);
+            }
             __syncwarp();
         }
 

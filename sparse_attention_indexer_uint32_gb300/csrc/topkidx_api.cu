@@ -37,7 +37,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
 // PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
 // 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
-topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -199,6 +199,64 @@ topk_status_t resident_warp_units(int* units) {
     return TOPK_OK;
 }
 
+// Launch shape of the warp-specialised single-block kernel: 24 KB copies in a
+// two-stage ring (the streaming warps' 8 x 32 lanes take 6 float4s each), two
+// candidate buffers of max(2560, 4k) entries.  At k <= 640 that is about
+// 111 KB of shared memory, two blocks per SM.
+// Whether the automatic dispatch takes the warp-specialised kernel.
+constexpr bool kStreamAuto = false;
+
+struct StreamConfig {
+    int tile, stages, cap, samples;
+    float gate_fill;
+    size_t smem;
+};
+
+StreamConfig stream_config(int32_t k, const topk_tuning_t& t) {
+    StreamConfig c;
+    c.tile = 6144;
+    c.stages = 2;
+    int cap = t.candidate_capacity;
+    if (cap == 0) {
+        cap = std::max(2560, 4 * k);
+        if (cap > 16384) cap = 16384;
+        cap = (cap + 63) / 64 * 64;
+    }
+    c.cap = cap;
+    int samples = t.samples;
+    if (samples == 0 || samples > kMaxSamples) samples = kMaxSamples;
+    c.samples = samples;
+    c.gate_fill = t.gate_fill_percent > 0 ? 0.01f * static_cast<float>(t.gate_fill_percent) : 0.4f;
+    c.smem = make_stream_layout(c.tile, c.stages, c.cap, k).total;
+    return c;
+}
+
+topk_status_t resident_stream_units(size_t smem, int* units) {
+    static std::map<std::pair<int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(dev, smem);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *units = it->second;
+            return TOPK_OK;
+        }
+    }
+    int u = 0;
+    const cudaError_t e = stream_select_occupancy(smem, &u);
+    if (e != cudaSuccess) return cuda_fail(e, "stream select occupancy query");
+    if (u <= 0) {
+        snprintf(g_last_error, sizeof(g_last_error), "stream select kernel (%zu B smem) cannot be resident", smem);
+        return TOPK_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    cache[key] = u;
+    *units = u;
+    return TOPK_OK;
+}
+
 // The kernels one topk_transform call launches.  Long rows go to the cluster
 // kernel.  Blocks per row (cluster_size 0): 16 while the rows take at most
 // one SM per block that way, 8 while every row gets a resident cluster at
@@ -299,6 +357,7 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (t->gate_refresh_tiles < 0 || t->gate_refresh_tiles > 64) return TOPK_EINVAL;
     if (t->warp_rows != 0 && t->warp_rows != 1) return TOPK_EINVAL;
     if (t->wait_limit_us < 0 || t->wait_limit_us > 60000000) return TOPK_EINVAL;
+    if (t->single_block_kernel < 0 || t->single_block_kernel > 2) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -391,7 +450,40 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         if (e != cudaSuccess) return cuda_fail(e, "warp select launch");
         return TOPK_OK;
     }
-    if (!fold_short) {
+    // The warp-specialised single-block kernel: forced, or automatic for rows
+    // over 16K when two of its blocks fit on an SM (and no option of the
+    // single-role kernel is asked for).
+    bool use_stream = false;
+    StreamConfig sc = {};
+    int stream_units = 0;
+    if (!fold_short && t.single_block_kernel != 1) {
+        sc = stream_config(k, t);
+        const topk_status_t r = resident_stream_units(sc.smem, &stream_units);
+        if (r != TOPK_OK) return r;
+        const bool classic_knobs = t.gate_refresh_tiles != 0 || t.single_block_threads != 0 ||
+                                   t.single_block_copy_bytes != 0 || t.single_block_stages != 0;
+        use_stream = t.single_block_kernel == 2 ||
+                     (kStreamAuto && max_seq_len > 16384 && stream_units >= 2 * sm_count() && !classic_knobs);
+    }
+    if (use_stream) {
+        SelectParams q = p;
+        q.items = plan_short_list(workspace, batch);
+        q.n_items_dev = &hdr->n_short;
+        if (!launch_long) {
+            q.items2 = plan_long_list(workspace);
+            q.n_items2_dev = &hdr->n_long;
+        }
+        q.tile = sc.tile;
+        q.stages = sc.stages;
+        q.gate_refresh = 0;
+        q.cap = sc.cap;
+        q.samples = sc.samples;
+        q.gate_fill = sc.gate_fill;
+        const int per_unit = (batch + stream_units - 1) / stream_units;
+        const int grid = (batch + per_unit - 1) / per_unit;
+        const cudaError_t e = launch_stream_select(q, grid, sc.smem, st);
+        if (e != cudaSuccess) return cuda_fail(e, "stream select launch");
+    } else if (!fold_short) {
         // The single-block kernel goes first: at small batch it usually has no
         // rows and ends as soon as the plan does, and a cluster kernel, placed
         // on the GPU meanwhile (programmatic launch), starts right after it.

@@ -181,7 +181,7 @@ def test_launch_count_query_matches_the_dispatch():
     assert lib.topk_transform_launches(4096, 262144, 512) == 2
 
 
-@pytest.mark.parametrize("path", ["single_block", "cluster"])
+@pytest.mark.parametrize("path", ["single_block", "stream", "cluster"])
 def test_bounded_wait_gives_up_and_the_next_call_is_correct(path):
     """A wait limit of 1 us is shorter than a bulk copy of scores takes, so the
     select blocks give up waiting: the call must return, the flag word must
@@ -200,7 +200,7 @@ def test_bounded_wait_gives_up_and_the_next_call_is_correct(path):
     else:
         wl = workloads.random_case(seed=800, batch=1200, min_len=40000, max_len=65536, k=512, page_size=64,
                                    dist="normal")
-        thr, extra = 1 << 30, {}
+        thr, extra = 1 << 30, dict(single_block_kernel=2 if path == "stream" else 1)
     # A wait runs out only when a copy takes longer than the limit after the
     # first probe, which a memory-bound launch of this size shows many times;
     # a few attempts keep the test independent of one launch's timing.
