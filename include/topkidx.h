@@ -222,13 +222,14 @@ const char* topk_last_error_string(void);
  * host thread is enqueuing topk_transform.
  */
 typedef struct {
-    int32_t long_threshold_small_batch; /* long row if seq_len > this, batch <= small_batch_max */
-    int32_t long_threshold;             /* long row if seq_len > this, larger batches           */
-    int32_t small_batch_max;            /* batch size up to which the small-batch threshold holds */
+    int32_t long_threshold_small_batch; /* long row if seq_len > this, batch <= small_batch_max
+                                           (16384)                                               */
+    int32_t long_threshold;             /* long row if seq_len > this, batch <= large_batch_min
+                                           (65536)                                               */
+    int32_t small_batch_max;            /* (16)                                                  */
     int32_t cluster_size;               /* blocks per long row: 2, 4, 8 or 16; 0: automatic (16
-                                           when batch x 16 is at most the SM count, 8 while every
-                                           row gets a resident cluster, else 4 unless the rows are
-                                           too long for 4-block buffers, then 8)                 */
+                                           for up to 4 rows, 8 while every row gets a resident
+                                           8-block cluster, else 4)                              */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every
                                            row takes the two-pass streaming path                  */
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */
@@ -251,20 +252,27 @@ typedef struct {
                                            tightens a row's gate every this many bulk copies from
                                            the counts of its histogram so far (a monotone gate that
                                            never drops a top-k element); other kernels ignore it  */
-    int32_t warp_rows;                  /* 0: off; 1: a batch whose rows are all at most 16384 long,
-                                           with k <= 512, goes to the warp-per-row kernel (one warp
-                                           per row; slower than the default on the 8192 x 8192
-                                           workload so far, hence off by default)                 */
+    int32_t warp_rows;                  /* the warp-per-row kernel (one warp per row) for batches
+                                           whose rows are all at most 16384 long, with k <= 512:
+                                           0: automatic (from wide_batch_min rows on); 1: always;
+                                           2: never                                              */
     int32_t wait_limit_us;              /* 0: 2 s; else 1..60000000: how long a select block waits
                                            for one bulk copy of scores before it gives up, sets
                                            TOPK_FLAG_TIMEOUT (the call's output is then void) and
                                            stops issuing copies; the call still returns, and the
                                            block waits for its copies in flight before it exits  */
-    int32_t single_block_kernel;        /* 0: automatic (the warp-specialised kernel for rows over
-                                           16384 when two of its blocks fit on an SM, else the
-                                           single-role kernel); 1: always the single-role kernel;
-                                           2: always the warp-specialised kernel, in which 8 warps
-                                           stream row q while 4 warps finish row q - 1           */
+    int32_t single_block_kernel;        /* 0: automatic (shape 2 for rows of 16K..64K from
+                                           wide_batch_min rows on, when two blocks fit on an SM);
+                                           1: the single-role kernel; 2 / 3: the warp-specialised
+                                           kernel, in which 8 warps stream row q while other warps
+                                           finish row q - 1: 2 = 4 finishing warps, a 2 x 24 KB
+                                           ring, two blocks per SM (k <= 640); 3 = 8 finishing
+                                           warps, up to 4 x 32 KB, one block per SM              */
+    int32_t long_threshold_large_batch; /* long row if seq_len > this, batch > large_batch_min
+                                           (131072)                                              */
+    int32_t large_batch_min;            /* (64)                                                  */
+    int32_t wide_batch_min;             /* batch from which the automatic dispatch takes the
+                                           warp-per-row and warp-specialised kernels (1024)      */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -71,6 +71,9 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("warp_rows", ctypes.c_int32),
         ("wait_limit_us", ctypes.c_int32),
         ("single_block_kernel", ctypes.c_int32),
+        ("long_threshold_large_batch", ctypes.c_int32),
+        ("large_batch_min", ctypes.c_int32),
+        ("wide_batch_min", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -158,17 +158,17 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
 }
 
 // The warp-specialised single-block kernel (topk_stream.cu): 8 streaming
-// warps run pass 1 of row q while 4 resolving warps finish row q - 1 and
-// compute the gate of row q + 1, with two candidate-buffer / histogram sets.
+// warps run pass 1 of row q while 4 or 8 resolving warps finish row q - 1
+// and compute the gate of row q + 1, with two candidate-buffer / histogram
+// sets.
 constexpr int kStreamWarps = 8;
-constexpr int kResolveWarps = 4;
-constexpr int kStreamThreads = 32 * (kStreamWarps + kResolveWarps);
 
 struct __align__(16) SetControl {
     uint32_t ncand[2];  // candidates in set b (pass 1, or a collect pass)
     uint32_t lo[2];     // gate key of the row held by set b
     uint32_t shift[2];  // bin shift of set b's first histogram
-    uint32_t pad[2];
+    uint32_t ncand_seen; // the resolving warps' snapshot of the row's candidate count
+    uint32_t pad;
 };
 
 struct StreamLayout {
@@ -231,8 +231,10 @@ cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, 
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream);
 cudaError_t launch_warp_select(const SelectParams& p, int grid, cudaStream_t stream);
 // The warp-specialised single-block kernel (topk_stream.cu).
-cudaError_t launch_stream_select(const SelectParams& p, int grid, size_t smem, cudaStream_t stream);
-cudaError_t stream_select_occupancy(size_t smem, int* units_out);
+// resolve_warps: 4 (two blocks per SM) or 8 (one block per SM).
+cudaError_t launch_stream_select(const SelectParams& p, int resolve_warps, int grid, size_t smem,
+                                 cudaStream_t stream);
+cudaError_t stream_select_occupancy(int resolve_warps, size_t smem, int* units_out);
 cudaError_t warp_select_occupancy(int* units_out);
 size_t warp_select_smem_bytes();
 

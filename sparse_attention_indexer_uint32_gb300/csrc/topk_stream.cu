@@ -49,16 +49,21 @@ using namespace detail;
 
 namespace {
 
-constexpr int kST = 32 * kStreamWarps;   // streaming threads
-constexpr int kRT = 32 * kResolveWarps;  // resolving threads
-using RSync = GroupSync<1, kRT>;         // barrier of the resolving warps only
-constexpr int kRSamples = kMaxSamples / kRT;
+constexpr int kST = 32 * kStreamWarps;  // streaming threads
 
 #define SCTL(base, field) ((base) + static_cast<uint32_t>(offsetof(SetControl, field)))
 
 }  // namespace
 
-__global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const SelectParams p) {
+// RW resolving warps: 4 (two blocks per SM, a two-stage ring) or 8 (one
+// block per SM, a deeper ring).
+template <int RW>
+__global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) stream_select_kernel(const SelectParams p) {
+    constexpr int kRT = 32 * RW;                      // resolving threads
+    constexpr int kThreads = kST + kRT;
+    constexpr int kRSamples = kMaxSamples / kRT;      // gate samples per resolving thread
+    static_assert(kRSamples % 4 == 0, "gate samples are loaded as float4s");
+    using RSync = GroupSync<1, kRT>;                  // barrier of the resolving warps only
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const StreamLayout lay = make_stream_layout(p.tile, p.stages, p.cap, p.k);
     const uint32_t sbase = ptx::smem_addr(smem_raw);
@@ -111,8 +116,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
         for (int b = 0; b < 2; ++b) ptx::sts_u32(SCTL(sctl, ncand) + 4u * b, 0);
         for (uint32_t i = 0; i < stages; ++i) ptx::sts_u32(claim + 4u * i, 0xffffffffu);
     }
-    clear_hist<kStreamThreads>(hist_of(0), tid);
-    clear_hist<kStreamThreads>(hist_of(1), tid);
+    clear_hist<kThreads>(hist_of(0), tid);
+    clear_hist<kThreads>(hist_of(1), tid);
     __syncthreads();
     // Every global access of this kernel comes after this point.
     ptx::grid_dependency_wait();
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
 
     for (int32_t w0 = 0; w0 < my_items; w0 += kItemsMax) {
         const int32_t nw = min(kItemsMax, my_items - w0);
-        for (int32_t i = tid; i < nw; i += kStreamThreads) {
+        for (int32_t i = tid; i < nw; i += kThreads) {
             const int32_t it = unit + (w0 + i) * nunits;
             const int32_t row = identity ? (it < n_first ? it : it - n_first)
                                          : (it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first]);
@@ -365,13 +370,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                                                : static_cast<uint32_t>(p.samples);
                 return min(m, L);
             };
-            auto prefetch_samples = [&](int32_t j) {
-                const uint32_t L = ptx::lds_u32(it_len + 4u * j);
-                const uint32_t M = samples_for(L);
-                const float* rowp = p.scores + static_cast<int64_t>(ptx::lds_u32(it_row + 4u * j)) * p.row_stride;
-                for (uint32_t seg = static_cast<uint32_t>(rtid); seg * 32u < M; seg += kRT)
-                    ptx::prefetch_l2(rowp + sample_pos(seg * 32u, L, M));
-            };
             auto publish_gate = [&](int32_t j, uint32_t b) {
                 const uint32_t hs = hist_of(b);
                 const uint32_t L = ptx::lds_u32(it_len + 4u * j);
@@ -388,19 +386,37 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                     const uint32_t r = static_cast<uint32_t>(r_f);
                     const float* rowp =
                         p.scores + static_cast<int64_t>(ptx::lds_u32(it_row + 4u * j)) * p.row_stride;
+                    // The samples come in 32-float segments: a thread loads float4
+                    // f = q * 128 + rtid, part f & 7 of segment f >> 3 (16-byte
+                    // loads, all issued before any is used).
                     uint32_t keys[kRSamples];
+                    uint32_t valid = 0;  // bit 4q + c: keys[4q + c] is a sample
                     uint32_t kmax = 0;
                     if (rtid == 0) ptx::sts_u32(CTL(s, smax), 0);
+                    {
+                        float4 sv[kRSamples / 4];
 #pragma unroll
-                    for (int q = 0; q < kRSamples; ++q) {
-                        const uint32_t i = static_cast<uint32_t>(q * kRT + rtid);
-                        keys[q] = i < M ? score_key(__ldg(rowp + sample_pos(i, L, M))) : 0u;
+                        for (int q = 0; q < kRSamples / 4; ++q) {
+                            const uint32_t f = static_cast<uint32_t>(q * kRT + rtid);
+                            const uint32_t i0 = (f >> 3) * 32u + (f & 7u) * 4u;  // first sample of the float4
+                            sv[q] = i0 < M ? __ldg(reinterpret_cast<const float4*>(
+                                                 rowp + sample_pos((f >> 3) * 32u, L, M) + (f & 7u) * 4u))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const uint32_t vq = i0 + 4u <= M ? 15u : (i0 >= M ? 0u : (1u << (M - i0)) - 1u);
+                            valid |= vq << (4 * q);
+                        }
+#pragma unroll
+                        for (int q = 0; q < kRSamples / 4; ++q) {
+                            keys[4 * q] = score_key(sv[q].x);
+                            keys[4 * q + 1] = score_key(sv[q].y);
+                            keys[4 * q + 2] = score_key(sv[q].z);
+                            keys[4 * q + 3] = score_key(sv[q].w);
+                        }
                     }
                     rsync();
 #pragma unroll
                     for (int q = 0; q < kRSamples; ++q) {
-                        const uint32_t i = static_cast<uint32_t>(q * kRT + rtid);
-                        if (i < M) {
+                        if ((valid >> q) & 1u) {
                             ptx::red_add_s(hs + 4u * (keys[q] >> (32 - kBinBits)), 1u);
                             kmax = max(kmax, keys[q]);
                         }
@@ -416,8 +432,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                         rsync();
 #pragma unroll
                         for (int q = 0; q < kRSamples; ++q) {
-                            const uint32_t i = static_cast<uint32_t>(q * kRT + rtid);
-                            if (i < M && (keys[q] >> (32 - kBinBits)) == g.bin)
+                            if (((valid >> q) & 1u) && (keys[q] >> (32 - kBinBits)) == g.bin)
                                 ptx::red_add_s(hs + 4u * ((keys[q] >> (32 - 2 * kBinBits)) & (kBins - 1)), 1u);
                         }
                         rsync();
@@ -448,8 +463,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
             {
                 const int32_t j0 = nth_select_item(-1, 1);
                 const int32_t j1 = j0 >= 0 ? nth_select_item(j0, 1) : -1;
-                if (j0 >= 0) prefetch_samples(j0);
-                if (j1 >= 0) prefetch_samples(j1);
                 if (j0 >= 0) publish_gate(j0, qslot & 1u);
                 if (j1 >= 0) publish_gate(j1, (qslot + 1u) & 1u);
             }
@@ -471,12 +484,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                 }
                 const uint32_t b = qslot & 1u;
                 const int32_t j_next = nth_select_item(j, 2);  // the row whose gate set b takes next
-                if (j_next >= 0) prefetch_samples(j_next);
                 if (rtid == 0) {
                     ptx::sts_u32(CTL(s, nemit), 0);
                     ptx::sts_u32(CTL(s, nfin), 0);
                 }
                 handover_wait(&done[b], (qslot >> 1) & 1u);
+                // Every decision of the resolving warps must be the same in all
+                // of them (they meet at group barriers): the candidate count is
+                // read once and shared.  (After a hand-over wait gave up, the
+                // streaming warps may still be adding to it.)
+                if (rtid == 0) ptx::sts_u32(SCTL(sctl, ncand_seen), ptx::lds_u32(SCTL(sctl, ncand) + 4u * b));
                 rsync();
 
                 // -------------------------------------------------- resolve
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                 const uint32_t ncand_addr = SCTL(sctl, ncand) + 4u * b;
                 const uint32_t lo = ptx::lds_u32(SCTL(sctl, lo) + 4u * b);
                 const int shift = static_cast<int>(ptx::lds_u32(SCTL(sctl, shift) + 4u * b));
-                const bool overflow = !buffering || ptx::lds_u32(ncand_addr) > cap;
+                const bool overflow = !buffering || ptx::lds_u32(SCTL(sctl, ncand_seen)) > cap;
                 const float* row_ptr = p.scores + static_cast<int64_t>(row) * p.row_stride;
                 const float4* row4 = reinterpret_cast<const float4*>(row_ptr);
                 const uint32_t nvec = (L + 3u) >> 2;
@@ -515,6 +532,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                 clear_hist<kRT>(hs, rtid);
                 rsync();
 
+                // The set's candidate count, the same in every resolving thread
+                // (loops that hold warp-wide ballots and shuffles take it as
+                // their bound; capped at the buffer).  Every resolving thread
+                // must call it.
+                auto group_count = [&]() -> uint32_t {
+                    rsync();
+                    if (rtid == 0) ptx::sts_u32(SCTL(sctl, ncand_seen), min(ptx::lds_u32(ncand_addr), cap));
+                    rsync();
+                    return ptx::lds_u32(SCTL(sctl, ncand_seen));
+                };
                 auto emit_warp = [&](bool flag, uint32_t idx) {
                     const uint32_t slot = warp_reserve(CTL(s, nemit), flag, lane);
                     if (flag) {
@@ -599,7 +626,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                     // One more 11-bit round over [r_lo, r_hi].
                     const int sh = shift_for_span(r_hi - r_lo);
                     if (!stream_mode) {
-                        const uint32_t nc = min(ptx::lds_u32(ncand_addr), cap);  // never past the buffer
+                        const uint32_t nc = group_count();
                         for (uint32_t i = rtid; i < nc; i += kRT) {
                             const uint32_t key = ptx::lds_u32(ck + 4u * i);
                             if (key >= r_lo && key <= r_hi) ptx::red_add_s(hs + 4u * ((key - r_lo) >> sh), 1u);
@@ -662,7 +689,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                     const uint32_t quota = need;
                     const bool all_eq = (quota == cnt);
                     if (!stream_mode) {
-                        const uint32_t nc = min(ptx::lds_u32(ncand_addr), cap);  // never past the buffer
+                        const uint32_t nc = group_count();
                         emit_from_buffer(nc, [&](uint32_t key) { return key > T || (all_eq && key == T); });
                         if (!all_eq && quota > 0) {
                             // The `quota` smallest positions among the copies of T:
@@ -752,7 +779,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                             if (lane == 31) ptx::sts_u32(s.warp_tot + 4u * rwarp, incl);
                             rsync();
                             uint32_t pre = 0, tot = 0;
-                            for (int w = 0; w < kResolveWarps; ++w) {
+                            for (int w = 0; w < RW; ++w) {
                                 const uint32_t t = ptx::lds_u32(s.warp_tot + 4u * w);
                                 pre += (w < rwarp) ? t : 0u;
                                 tot += t;
@@ -771,7 +798,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
                 } else {
                     // ---- <= 32 candidates in [r_lo, r_hi]: warp compare-and-swap finish
                     const bool take_range = need >= cnt;
-                    const uint32_t nc = min(ptx::lds_u32(ncand_addr), cap);  // never past the buffer
+                    const uint32_t nc = group_count();
                     for (uint32_t i0 = 0; i0 < nc; i0 += 4u * kRT) {
                         uint32_t key[4], pos[4];
                         uint32_t m = 0, f = 0;
@@ -857,6 +884,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) stream_select_kernel(const 
 
 namespace {
 
+template <int RW>
 cudaError_t stream_attributes() {
     static std::atomic<uint64_t> done{0};
     int dev = 0;
@@ -867,20 +895,19 @@ cudaError_t stream_attributes() {
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(stream_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    e = cudaFuncSetAttribute(stream_select_kernel<RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_release);
     return cudaSuccess;
 }
 
-}  // namespace
-
-cudaError_t launch_stream_select(const SelectParams& p, int grid, size_t smem, cudaStream_t stream) {
-    const cudaError_t ea = stream_attributes();
+template <int RW>
+cudaError_t launch_stream_t(const SelectParams& p, int grid, size_t smem, cudaStream_t stream) {
+    const cudaError_t ea = stream_attributes<RW>();
     if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kStreamThreads);
+    cfg.blockDim = dim3(32 * (kStreamWarps + RW));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -888,19 +915,32 @@ cudaError_t launch_stream_select(const SelectParams& p, int grid, size_t smem, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stream_select_kernel, p);
+    return cudaLaunchKernelEx(&cfg, stream_select_kernel<RW>, p);
 }
 
-cudaError_t stream_select_occupancy(size_t smem, int* units_out) {
-    cudaError_t e = stream_attributes();
+template <int RW>
+cudaError_t stream_occupancy_t(size_t smem, int* units_out) {
+    cudaError_t e = stream_attributes<RW>();
     if (e != cudaSuccess) return e;
     int per_sm = 0, dev = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_select_kernel, kStreamThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_select_kernel<RW>, 32 * (kStreamWarps + RW),
+                                                      smem);
     if (e != cudaSuccess) return e;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     *units_out = per_sm * sms;
     return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_stream_select(const SelectParams& p, int resolve_warps, int grid, size_t smem,
+                                 cudaStream_t stream) {
+    return resolve_warps == 8 ? launch_stream_t<8>(p, grid, smem, stream) : launch_stream_t<4>(p, grid, smem, stream);
+}
+
+cudaError_t stream_select_occupancy(int resolve_warps, size_t smem, int* units_out) {
+    return resolve_warps == 8 ? stream_occupancy_t<8>(smem, units_out) : stream_occupancy_t<4>(smem, units_out);
 }
 
 }  // namespace topkidx

@@ -32,12 +32,18 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
     return TOPK_ECUDA;
 }
 
-// Thresholds after SGLang PR #26788 (commit "Fuse the cluster/non-cluster
-// split for small batch": long rows above 32K for small batches, 64K
-// otherwise; raised from batch <= 8 to <= 15 in a later commit of the same
-// PR).  Blocks per long row: chosen per call (cluster_size 0) from the batch:
-// 16, 8 (the cluster size both the PR and the DistRadixTopK README use) or 4.
-topk_tuning_t g_tuning = {32768, 65536, 15, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+// Dispatch defaults, from a sweep of batch x seq_len x k on GB300 (every path
+// timed, plan + transform replayed from a graph, L2 flushed; the table is in
+// the design notes).  Long rows (one cluster per row): above 16K for batches
+// of up to 16 rows, above 64K up to 64 rows, above 128K for larger batches
+// -- the batch-dependent floor of SGLang PR #26788 (commits "Fuse the
+// cluster/non-cluster split for small batch" and its later floor change)
+// with the seq-dependent cap of the same PR expressed as a third tier: at
+// batch 128 x 128K one block per row is 1.3-1.8x faster than clusters, at
+// 256K clusters win at every batch.  From 1024 rows on, short rows (<= 16K,
+// k <= 512) go to the warp-per-row kernel and mid rows (<= 64K, k <= 640) to
+// the warp-specialised kernel (1.1-1.6x on those shapes).
+topk_tuning_t g_tuning = {16384, 65536, 16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 131072, 64, 1024};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -65,7 +71,8 @@ topk_status_t check_device() {
 }
 
 int32_t long_threshold(const topk_tuning_t& t, int32_t batch) {
-    return batch <= t.small_batch_max ? t.long_threshold_small_batch : t.long_threshold;
+    if (batch <= t.small_batch_max) return t.long_threshold_small_batch;
+    return batch <= t.large_batch_min ? t.long_threshold : t.long_threshold_large_batch;
 }
 
 struct PathConfig {
@@ -199,26 +206,25 @@ topk_status_t resident_warp_units(int* units) {
     return TOPK_OK;
 }
 
-// Launch shape of the warp-specialised single-block kernel: 24 KB copies in a
-// two-stage ring (the streaming warps' 8 x 32 lanes take 6 float4s each), two
-// candidate buffers of max(2560, 4k) entries.  At k <= 640 that is about
-// 111 KB of shared memory, two blocks per SM.
-// Whether the automatic dispatch takes the warp-specialised kernel.
-constexpr bool kStreamAuto = false;
-
+// Launch shapes of the warp-specialised single-block kernel.  Two candidate
+// buffers of max(2560, 4k) entries (shape 2) or max(3072, 4k) (shape 3).
+//  - shape 2: 4 resolving warps, 24 KB copies in a two-stage ring: about
+//    111 KB of shared memory at k <= 640, two blocks per SM;
+//  - shape 3: 8 resolving warps, 32 KB copies in a ring as deep as the
+//    shared memory allows (up to four stages), one block per SM.
 struct StreamConfig {
-    int tile, stages, cap, samples;
+    int resolve_warps, tile, stages, cap, samples;
     float gate_fill;
     size_t smem;
 };
 
-StreamConfig stream_config(int32_t k, const topk_tuning_t& t) {
+StreamConfig stream_config(int shape, int32_t k, const topk_tuning_t& t) {
     StreamConfig c;
-    c.tile = 6144;
-    c.stages = 2;
+    c.resolve_warps = shape == 3 ? 8 : 4;
+    c.tile = shape == 3 ? 8192 : 6144;
     int cap = t.candidate_capacity;
     if (cap == 0) {
-        cap = std::max(2560, 4 * k);
+        cap = std::max(shape == 3 ? 3072 : 2560, 4 * k);
         if (cap > 16384) cap = 16384;
         cap = (cap + 63) / 64 * 64;
     }
@@ -227,15 +233,29 @@ StreamConfig stream_config(int32_t k, const topk_tuning_t& t) {
     if (samples == 0 || samples > kMaxSamples) samples = kMaxSamples;
     c.samples = samples;
     c.gate_fill = t.gate_fill_percent > 0 ? 0.01f * static_cast<float>(t.gate_fill_percent) : 0.4f;
+    c.stages = 2;
+    // Explicit copy size and ring depth (a copy is 2, 4, 6 or 8 float4s per
+    // streaming thread).
+    const int tile = t.single_block_copy_bytes / 4;
+    const int v = tile / (4 * 32 * kStreamWarps);
+    if (tile > 0 && v * 4 * 32 * kStreamWarps == tile && (v == 2 || v == 4 || v == 6 || v == 8)) c.tile = tile;
+    if (t.single_block_stages > 0) c.stages = t.single_block_stages;
+    if (shape == 3 && t.single_block_stages == 0) {
+        int dev = 0, optin = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        while (c.stages < 4 && make_stream_layout(c.tile, c.stages + 1, c.cap, k).total <= static_cast<uint32_t>(optin))
+            ++c.stages;
+    }
     c.smem = make_stream_layout(c.tile, c.stages, c.cap, k).total;
     return c;
 }
 
-topk_status_t resident_stream_units(size_t smem, int* units) {
+topk_status_t resident_stream_units(int resolve_warps, size_t smem, int* units) {
     static std::map<std::pair<int, size_t>, int> cache;
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_pair(dev, smem);
+    const auto key = std::make_pair(dev * 16 + resolve_warps, smem);
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         auto it = cache.find(key);
@@ -245,7 +265,7 @@ topk_status_t resident_stream_units(size_t smem, int* units) {
         }
     }
     int u = 0;
-    const cudaError_t e = stream_select_occupancy(smem, &u);
+    const cudaError_t e = stream_select_occupancy(resolve_warps, smem, &u);
     if (e != cudaSuccess) return cuda_fail(e, "stream select occupancy query");
     if (u <= 0) {
         snprintf(g_last_error, sizeof(g_last_error), "stream select kernel (%zu B smem) cannot be resident", smem);
@@ -278,27 +298,17 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
     if (!d->launch_long) return TOPK_OK;
     int cluster = t.cluster_size;
     if (cluster == 0) {
-        if (static_cast<int64_t>(batch) * 16 <= sm_count()) {
+        // 16 blocks per row for up to 4 rows, 8 while every row gets a resident
+        // 8-block cluster at once, else 4 (the sweep: 8 beats 16 from 8 rows
+        // on, 4 beats 8 once the rows exceed one wave of 8-block clusters).
+        if (batch <= 4 && static_cast<int64_t>(batch) * 16 <= sm_count()) {
             cluster = 16;
         } else {
             const PathConfig c8 = path_config(8, k, batch, max_seq_len, t);
             int u8 = 0;
             const topk_status_t r = resident_units(8, c8.threads, c8.smem, &u8);
             if (r != TOPK_OK) return r;
-            cluster = 8;
-            if (batch > u8) {
-                // 4 blocks per row unless the sampled gate's floor would crowd a
-                // block's candidate buffer: the gate passes at least about
-                // r_safe / M of a row (r_safe = E + 4 sqrt(E) + 4, E = M k / L),
-                // and a buffer should hold twice a block's share of that.
-                const PathConfig c4 = path_config(4, k, batch, max_seq_len, t);
-                const double L = static_cast<double>(max_seq_len);
-                const double M = L <= 16384.0 ? std::min(1024.0, static_cast<double>(c4.samples))
-                                              : static_cast<double>(c4.samples);
-                const double E = M * std::min(static_cast<double>(k), L) / L;
-                const double floor_per_block = (E + 4.0 * std::sqrt(E) + 4.0) * L / (M * 4.0);
-                if (2.0 * floor_per_block <= static_cast<double>(c4.cap)) cluster = 4;
-            }
+            cluster = batch <= u8 ? 8 : 4;
         }
     }
     d->cl = path_config(cluster, k, batch, max_seq_len, t);
@@ -337,7 +347,9 @@ topk_status_t topk_get_tuning(topk_tuning_t* tuning_host) {
 
 topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (!t) return TOPK_EINVAL;
-    if (t->long_threshold_small_batch < 0 || t->long_threshold < 0 || t->small_batch_max < 0) return TOPK_EINVAL;
+    if (t->long_threshold_small_batch < 0 || t->long_threshold < 0 || t->small_batch_max < 0 ||
+        t->long_threshold_large_batch < 0 || t->large_batch_min < 0 || t->wide_batch_min < 0)
+        return TOPK_EINVAL;
     if (t->cluster_size != 0 && t->cluster_size != 2 && t->cluster_size != 4 && t->cluster_size != 8 &&
         t->cluster_size != 16)
         return TOPK_EINVAL;
@@ -355,9 +367,9 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
         return TOPK_EINVAL;
     if (t->single_block_stages != 0 && (t->single_block_stages < 2 || t->single_block_stages > 8)) return TOPK_EINVAL;
     if (t->gate_refresh_tiles < 0 || t->gate_refresh_tiles > 64) return TOPK_EINVAL;
-    if (t->warp_rows != 0 && t->warp_rows != 1) return TOPK_EINVAL;
+    if (t->warp_rows < 0 || t->warp_rows > 2) return TOPK_EINVAL;
     if (t->wait_limit_us < 0 || t->wait_limit_us > 60000000) return TOPK_EINVAL;
-    if (t->single_block_kernel < 0 || t->single_block_kernel > 2) return TOPK_EINVAL;
+    if (t->single_block_kernel < 0 || t->single_block_kernel > 3) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -429,9 +441,11 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     const bool fold_short = d.fold_short;
     const PathConfig& cl = d.cl;
     const int cl_units = d.cl_units;
-    // Short rows, when asked for: the warp-per-row kernel takes every row.
-    const bool warp_ok = t.warp_rows == 1 && !launch_long && !fold_short &&
-                         max_seq_len <= static_cast<int32_t>(kWarpMaxLen) && k <= kWarpMaxK;
+    // Short rows in a wide batch (or when asked for): the warp-per-row kernel
+    // takes every row.
+    const bool warp_fits = !launch_long && !fold_short && max_seq_len <= static_cast<int32_t>(kWarpMaxLen) &&
+                           k <= kWarpMaxK;
+    const bool warp_ok = warp_fits && (t.warp_rows == 1 || (t.warp_rows == 0 && batch >= t.wide_batch_min));
     if (warp_ok) {
         int warp_units = 0;
         {
@@ -457,13 +471,19 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     StreamConfig sc = {};
     int stream_units = 0;
     if (!fold_short && t.single_block_kernel != 1) {
-        sc = stream_config(k, t);
-        const topk_status_t r = resident_stream_units(sc.smem, &stream_units);
-        if (r != TOPK_OK) return r;
         const bool classic_knobs = t.gate_refresh_tiles != 0 || t.single_block_threads != 0 ||
                                    t.single_block_copy_bytes != 0 || t.single_block_stages != 0;
-        use_stream = t.single_block_kernel == 2 ||
-                     (kStreamAuto && max_seq_len > 16384 && stream_units >= 2 * sm_count() && !classic_knobs);
+        int shape = t.single_block_kernel;
+        const bool auto_fit = shape == 0 && !classic_knobs && max_seq_len > 16384 && max_seq_len <= 65536 &&
+                              batch >= t.wide_batch_min;
+        if (auto_fit) shape = 2;
+        if (shape >= 2) {
+            sc = stream_config(shape, k, t);
+            const topk_status_t r = resident_stream_units(sc.resolve_warps, sc.smem, &stream_units);
+            if (r != TOPK_OK) return r;
+            // automatic only where two blocks fit on an SM (k <= 640)
+            use_stream = !auto_fit || stream_units >= 2 * sm_count();
+        }
     }
     if (use_stream) {
         SelectParams q = p;
@@ -481,7 +501,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         q.gate_fill = sc.gate_fill;
         const int per_unit = (batch + stream_units - 1) / stream_units;
         const int grid = (batch + per_unit - 1) / per_unit;
-        const cudaError_t e = launch_stream_select(q, grid, sc.smem, st);
+        const cudaError_t e = launch_stream_select(q, sc.resolve_warps, grid, sc.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "stream select launch");
     } else if (!fold_short) {
         // The single-block kernel goes first: at small batch it usually has no

@@ -66,6 +66,9 @@ def tuning(**overrides):
 
     old = _lib.topk_get_tuning()
     new = _lib.topk_tuning_t(**old.as_dict())
+    if "long_threshold" in overrides and "long_threshold_large_batch" not in overrides:
+        # one threshold for every batch above the small-batch tier
+        overrides = {**overrides, "long_threshold_large_batch": overrides["long_threshold"]}
     for k, v in overrides.items():
         setattr(new, k, v)
     _lib.topk_set_tuning(new)

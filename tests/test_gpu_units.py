@@ -99,7 +99,8 @@ def test_plan_lists_match_oracle_classification():
         host = ws.cpu().numpy()
         hdr = host[:64].view(np.int32)
         t = lib.topk_get_tuning()
-        thr = t.long_threshold_small_batch if batch <= t.small_batch_max else t.long_threshold
+        thr = (t.long_threshold_small_batch if batch <= t.small_batch_max
+               else t.long_threshold if batch <= t.large_batch_min else t.long_threshold_large_batch)
         eff, is_long, flags = oracle.plan_classify(lens, max_len, thr)
         n_long, n_short = int(hdr[4]), int(hdr[5])
         lists = host[64:64 + 8 * batch].view(np.int32)
