@@ -265,9 +265,11 @@ typedef struct {
                                            wide_batch_min rows on, when two blocks fit on an SM);
                                            1: the single-role kernel; 2 / 3: the warp-specialised
                                            kernel, in which 8 warps stream row q while other warps
-                                           finish row q - 1: 2 = 4 finishing warps, a 2 x 24 KB
+                                           finish row q - 1: 2 = 4 finishing warps, a 2 x 28 KB
                                            ring, two blocks per SM (k <= 640); 3 = 8 finishing
-                                           warps, up to 4 x 32 KB, one block per SM              */
+                                           warps, up to 4 x 32 KB, one block per SM.  It takes
+                                           rows of up to 65536; longer ones use the single-role
+                                           kernel whatever this field says                       */
     int32_t long_threshold_large_batch; /* long row if seq_len > this, batch > large_batch_min
                                            (131072)                                              */
     int32_t large_batch_min;            /* (64)                                                  */

@@ -163,9 +163,11 @@ struct Smem {
 // Addresses of Control fields.
 #define CTL(s, field) ((s).ctl + static_cast<uint32_t>(offsetof(Control, field)))
 
-template <int NT>
+// Clears N (default: the histogram with its cluster-merge slots) counters.
+template <int NT, int N = kBinsX>
 __device__ __forceinline__ void clear_hist(uint32_t h, int tid) {
-    for (int i = tid * 4; i < kBinsX; i += NT * 4) ptx::sts_u4(h + 4u * i, make_uint4(0, 0, 0, 0));
+    static_assert(N % 4 == 0, "whole uint4s");
+    for (int i = tid * 4; i < N; i += NT * 4) ptx::sts_u4(h + 4u * i, make_uint4(0, 0, 0, 0));
 }
 
 // Finds, in a histogram whose bins are ordered by key, the bin where the
@@ -275,6 +277,23 @@ __device__ __forceinline__ uint32_t sample_pos(uint32_t i, uint32_t L, uint32_t 
     const uint64_t frac = static_cast<uint64_t>(seg * 0x9E3779B9u);
     const uint32_t start = static_cast<uint32_t>((frac * static_cast<uint64_t>(L - 31u)) >> 32) & ~3u;
     return start + (i & 31u);
+}
+
+// Work items of a persistent grid of `nunits` units (blocks, or clusters):
+// in round r, unit u takes item u + r * nunits when r is even and
+// (r + 1) * nunits - 1 - u when r is odd -- a boustrophedon over the plan's
+// longest-first list, so that a unit which took one of the longest rows in
+// one round takes one of the shortest in the next.
+__host__ __device__ __forceinline__ int32_t snake_item(int32_t unit, int32_t round, int32_t nunits) {
+    return (round & 1) ? (round + 1) * nunits - 1 - unit : unit + round * nunits;
+}
+
+// Items unit u takes out of n_items under snake_item.
+__host__ __device__ __forceinline__ int32_t snake_count(int32_t unit, int32_t n_items, int32_t nunits) {
+    const int32_t full = n_items / nunits, rem = n_items - full * nunits;
+    if (rem == 0) return full;
+    const bool covered = (full & 1) ? (unit >= nunits - rem) : (unit < rem);
+    return full + (covered ? 1 : 0);
 }
 
 }  // namespace detail

@@ -162,6 +162,8 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
 // and compute the gate of row q + 1, with two candidate-buffer / histogram
 // sets.
 constexpr int kStreamWarps = 8;
+constexpr int kStreamItemsMax = 64;     // work items per window of the warp-specialised kernel
+constexpr int32_t kStreamMaxLen = 65536;  // longest row it takes (16-bit candidate positions)
 
 struct __align__(16) SetControl {
     uint32_t ncand[2];  // candidates in set b (pass 1, or a collect pass)
@@ -181,15 +183,15 @@ __host__ __device__ inline StreamLayout make_stream_layout(int tile, int stages,
     uint32_t o = 0;
     l.ring = o;
     o = align_up(o + static_cast<uint32_t>(stages) * tile * 4u, 128);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 2; ++b) {  // no cluster-merge slots: kBins bins
         l.hist[b] = o;
-        o += kBinsX * 4u;
+        o += kBins * 4u;
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 2; ++b) {  // 32-bit keys, 16-bit positions
         l.cand_key[b] = o;
         o += static_cast<uint32_t>(cap) * 4u;
         l.cand_idx[b] = o;
-        o += static_cast<uint32_t>(cap) * 4u;
+        o += align_up(static_cast<uint32_t>(cap) * 2u, 16);
     }
     l.emit = o;
     o += align_up(static_cast<uint32_t>(k), 4) * 4u;
@@ -204,13 +206,13 @@ __host__ __device__ inline StreamLayout make_stream_layout(int tile, int stages,
     l.sctl = o;
     o += align_up(sizeof(SetControl), 16);
     l.items_row = o;
-    o += kItemsMax * 4u;
+    o += kStreamItemsMax * 4u;
     l.items_len = o;
-    o += kItemsMax * 4u;
+    o += kStreamItemsMax * 4u;
     l.items_tiles = o;
-    o += kItemsMax * 4u;
+    o += kStreamItemsMax * 4u;
     l.items_tile_start = o;
-    o += kItemsMax * 4u;
+    o += kStreamItemsMax * 4u;
     l.claim = o;
     o += align_up(static_cast<uint32_t>(stages), 4) * 4u;
     l.mbar = align_up(o, 8);

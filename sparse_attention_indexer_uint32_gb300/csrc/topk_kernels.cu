@@ -140,9 +140,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     const bool identity = p.plan && p.plan->identity;  // the plan wrote no lists: item i is row i
     const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
     const int32_t n_items = n_first + max(n_second, 0);
-    const int32_t my_items = n_items > static_cast<int32_t>(unit)
-                                 ? (n_items - 1 - static_cast<int32_t>(unit)) / static_cast<int32_t>(nunits) + 1
-                                 : 0;
+    const int32_t my_items = snake_count(static_cast<int32_t>(unit), n_items, static_cast<int32_t>(nunits));
     if (my_items <= 0) return;  // same for every block of a cluster
 
     const uint32_t K = static_cast<uint32_t>(p.k);
@@ -173,7 +171,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     for (int32_t w0 = 0; w0 < my_items; w0 += kItemsMax) {
         const int32_t nw = min(kItemsMax, my_items - w0);
         for (int32_t i = tid; i < nw; i += NT) {
-            const int32_t it = static_cast<int32_t>(unit) + (w0 + i) * static_cast<int32_t>(nunits);
+            const int32_t it = snake_item(static_cast<int32_t>(unit), w0 + i, static_cast<int32_t>(nunits));
             const int32_t row = identity ? (it < n_first ? it : it - n_first)
                                          : (it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first]);
             int32_t L = -1;

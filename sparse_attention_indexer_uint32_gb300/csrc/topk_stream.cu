@@ -10,7 +10,8 @@
 //  * 8 streaming warps run pass 1 only: every row's tiles come through the
 //    bulk-copy ring; each element is tested against the row's gate, and the
 //    ones that pass are keyed, counted in the row's 2048-bin histogram and
-//    kept (key, position) in the row's candidate buffer.
+//    kept (32-bit key, 16-bit position: rows of up to 65536) in the row's
+//    candidate buffer.
 //  * 4 resolving warps do the rest, one row behind: the histogram scan, the
 //    refinement rounds over the candidate buffer, the finish of the last <= 32
 //    candidates, the page-table gather and the output; then the sampled gate
@@ -116,8 +117,8 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
         for (int b = 0; b < 2; ++b) ptx::sts_u32(SCTL(sctl, ncand) + 4u * b, 0);
         for (uint32_t i = 0; i < stages; ++i) ptx::sts_u32(claim + 4u * i, 0xffffffffu);
     }
-    clear_hist<kThreads>(hist_of(0), tid);
-    clear_hist<kThreads>(hist_of(1), tid);
+    clear_hist<kThreads, kBins>(hist_of(0), tid);
+    clear_hist<kThreads, kBins>(hist_of(1), tid);
     __syncthreads();
     // Every global access of this kernel comes after this point.
     ptx::grid_dependency_wait();
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
     const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
     const int32_t n_items = n_first + max(n_second, 0);
     const int32_t unit = static_cast<int32_t>(blockIdx.x), nunits = static_cast<int32_t>(gridDim.x);
-    const int32_t my_items = n_items > unit ? (n_items - 1 - unit) / nunits + 1 : 0;
+    const int32_t my_items = snake_count(unit, n_items, nunits);
     if (my_items <= 0) return;
 
     const uint32_t K = static_cast<uint32_t>(p.k);
@@ -153,10 +154,10 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
     // Row slots handed out so far (both roles count the rows that need a select alike).
     uint32_t qslot = 0;
 
-    for (int32_t w0 = 0; w0 < my_items; w0 += kItemsMax) {
-        const int32_t nw = min(kItemsMax, my_items - w0);
+    for (int32_t w0 = 0; w0 < my_items; w0 += kStreamItemsMax) {
+        const int32_t nw = min(kStreamItemsMax, my_items - w0);
         for (int32_t i = tid; i < nw; i += kThreads) {
-            const int32_t it = unit + (w0 + i) * nunits;
+            const int32_t it = snake_item(unit, w0 + i, nunits);
             const int32_t row = identity ? (it < n_first ? it : it - n_first)
                                          : (it < n_first ? (p.items ? p.items[it] : it) : p.items2[it - n_first]);
             int32_t L = -1;
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                                     ptx::red_add_s(
                                         hs + 4u * min((key - lo) >> shift, static_cast<uint32_t>(kBins - 1)), 1u);
                                 ptx::sts_u32(ck + 4u * slot, pass ? key : 0u);
-                                ptx::sts_u32(ci + 4u * slot, base_idx + idx_in_tile);
+                                ptx::sts_u16(ci + 2u * slot, base_idx + idx_in_tile);
                                 ++slot;
                             }
                         } else {
@@ -346,6 +347,8 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                 };
                 if (vec_per_tile == 8u)
                     pass1(std::integral_constant<int, 8>{});
+                else if (vec_per_tile == 7u)
+                    pass1(std::integral_constant<int, 7>{});
                 else if (vec_per_tile == 6u)
                     pass1(std::integral_constant<int, 6>{});
                 else if (vec_per_tile == 4u)
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                     lo = g.bin << (32 - kBinBits);
                     if (g.above + g.count > r + r / 4u + 4u && g.count > 1u) {
                         // Refine inside the coarse bin on the next 11 bits.
-                        clear_hist<kRT>(hs, rtid);
+                        clear_hist<kRT, kBins>(hs, rtid);
                         rsync();
 #pragma unroll
                         for (int q = 0; q < kRSamples; ++q) {
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                     const uint32_t smax = ptx::lds_u32(CTL(s, smax));
                     const int bl = bit_length(smax - lo);
                     shift = bl > kBinBits - 1 ? bl - (kBinBits - 1) : 0;
-                    clear_hist<kRT>(hs, rtid);
+                    clear_hist<kRT, kBins>(hs, rtid);
                 }
                 if (rtid == 0) {
                     ptx::sts_u32(SCTL(sctl, lo) + 4u * b, lo);
@@ -529,7 +532,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                     cnt = sr.count;
                     stream_mode = overflow;
                 }
-                clear_hist<kRT>(hs, rtid);
+                clear_hist<kRT, kBins>(hs, rtid);
                 rsync();
 
                 // The set's candidate count, the same in every resolving thread
@@ -560,7 +563,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                             const uint32_t i = i0 + q * kRT + rtid;
                             const bool in = i < nc;
                             const uint32_t key = in ? ptx::lds_u32(ck + 4u * i) : 0u;
-                            pos[q] = in ? ptx::lds_u32(ci + 4u * i) : 0u;
+                            pos[q] = in ? ptx::lds_u16(ci + 2u * i) : 0u;
                             if (in && take(key)) m |= 1u << q;
                         }
                         uint32_t slot = warp_reserve_n(CTL(s, nemit), __popc(m), lane);
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                                     if (keep) {
                                         if (slot < cap) {
                                             ptx::sts_u32(ck + 4u * slot, key);
-                                            ptx::sts_u32(ci + 4u * slot, idx);
+                                            ptx::sts_u16(ci + 2u * slot, idx);
                                         } else {
                                             set_err(TOPK_FLAG_INTERNAL);
                                         }
@@ -666,7 +669,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                     sr = scan_find<kRT>(s, hs, Kp - G, rtid, 0, rsync);
                     if (sr.bin >= static_cast<uint32_t>(kBins)) {  // cannot happen: the range holds >= need
                         set_err(TOPK_FLAG_INTERNAL);
-                        clear_hist<kRT>(hs, rtid);
+                        clear_hist<kRT, kBins>(hs, rtid);
                         rsync();
                         break;
                     }
@@ -677,7 +680,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                     r_lo = nlo;
                     r_hi = nhi;
                     cnt = sr.count;
-                    clear_hist<kRT>(hs, rtid);
+                    clear_hist<kRT, kBins>(hs, rtid);
                     rsync();
                 }
                 rsync();
@@ -699,7 +702,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                                 if (v_lo == v_hi || v_cnt <= static_cast<uint32_t>(kFinish)) break;
                                 const int sh = shift_for_span(v_hi - v_lo);
                                 for (uint32_t i = rtid; i < nc; i += kRT) {
-                                    const uint32_t v = ~ptx::lds_u32(ci + 4u * i);
+                                    const uint32_t v = ~ptx::lds_u16(ci + 2u * i);
                                     if (ptx::lds_u32(ck + 4u * i) == T && v >= v_lo && v <= v_hi)
                                         ptx::red_add_s(hs + 4u * ((v - v_lo) >> sh), 1u);
                                 }
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                                 v_lo = nlo;
                                 v_hi = nhi;
                                 v_cnt = vs.count;
-                                clear_hist<kRT>(hs, rtid);
+                                clear_hist<kRT, kBins>(hs, rtid);
                                 rsync();
                             }
                             if (rtid == 0) ptx::sts_u32(CTL(s, nfin), 0);
@@ -720,7 +723,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                             for (uint32_t i0 = rwarp * 32u; i0 < nc; i0 += kRT) {
                                 const uint32_t i = i0 + lane;
                                 const bool eq = i < nc && ptx::lds_u32(ck + 4u * i) == T;
-                                const uint32_t pos = eq ? ptx::lds_u32(ci + 4u * i) : 0u;
+                                const uint32_t pos = eq ? ptx::lds_u16(ci + 2u * i) : 0u;
                                 const uint32_t v = ~pos;
                                 emit_warp(eq && v > v_hi, pos);
                                 const bool fin = eq && v >= v_lo && v <= v_hi;
@@ -807,7 +810,7 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
                             const uint32_t i = i0 + q * kRT + rtid;
                             const bool in = i < nc;
                             key[q] = in ? ptx::lds_u32(ck + 4u * i) : 0u;
-                            pos[q] = in ? ptx::lds_u32(ci + 4u * i) : 0u;
+                            pos[q] = in ? ptx::lds_u16(ci + 2u * i) : 0u;
                             const bool in_range = in && key[q] >= r_lo && key[q] <= r_hi;
                             if ((in && key[q] > r_hi) || (take_range && in_range)) m |= 1u << q;
                             if (!take_range && in_range) f |= 1u << q;

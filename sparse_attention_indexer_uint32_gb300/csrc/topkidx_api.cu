@@ -207,9 +207,10 @@ topk_status_t resident_warp_units(int* units) {
 }
 
 // Launch shapes of the warp-specialised single-block kernel.  Two candidate
-// buffers of max(2560, 4k) entries (shape 2) or max(3072, 4k) (shape 3).
-//  - shape 2: 4 resolving warps, 24 KB copies in a two-stage ring: about
-//    111 KB of shared memory at k <= 640, two blocks per SM;
+// buffers of max(2560, 4k) entries (shape 2) or max(3072, 4k) (shape 3), of
+// 6 bytes each (rows of up to 65536).
+//  - shape 2: 4 resolving warps, 28 KB copies in a two-stage ring: about
+//    106 KB of shared memory at k <= 640, two blocks per SM;
 //  - shape 3: 8 resolving warps, 32 KB copies in a ring as deep as the
 //    shared memory allows (up to four stages), one block per SM.
 struct StreamConfig {
@@ -221,7 +222,7 @@ struct StreamConfig {
 StreamConfig stream_config(int shape, int32_t k, const topk_tuning_t& t) {
     StreamConfig c;
     c.resolve_warps = shape == 3 ? 8 : 4;
-    c.tile = shape == 3 ? 8192 : 6144;
+    c.tile = shape == 3 ? 8192 : 7168;
     int cap = t.candidate_capacity;
     if (cap == 0) {
         cap = std::max(shape == 3 ? 3072 : 2560, 4 * k);
@@ -238,7 +239,8 @@ StreamConfig stream_config(int shape, int32_t k, const topk_tuning_t& t) {
     // streaming thread).
     const int tile = t.single_block_copy_bytes / 4;
     const int v = tile / (4 * 32 * kStreamWarps);
-    if (tile > 0 && v * 4 * 32 * kStreamWarps == tile && (v == 2 || v == 4 || v == 6 || v == 8)) c.tile = tile;
+    if (tile > 0 && v * 4 * 32 * kStreamWarps == tile && (v == 2 || v == 4 || v == 6 || v == 7 || v == 8))
+        c.tile = tile;
     if (t.single_block_stages > 0) c.stages = t.single_block_stages;
     if (shape == 3 && t.single_block_stages == 0) {
         int dev = 0, optin = 0;
@@ -473,9 +475,12 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     if (!fold_short && t.single_block_kernel != 1) {
         const bool classic_knobs = t.gate_refresh_tiles != 0 || t.single_block_threads != 0 ||
                                    t.single_block_copy_bytes != 0 || t.single_block_stages != 0;
-        int shape = t.single_block_kernel;
-        const bool auto_fit = shape == 0 && !classic_knobs && max_seq_len > 16384 && max_seq_len <= 65536 &&
-                              batch >= t.wide_batch_min;
+        // The longest row the single-block launch takes (the short list only,
+        // when a cluster launch takes the long rows); the warp-specialised
+        // kernel keeps 16-bit positions, so it takes rows of up to 65536.
+        const int32_t longest = launch_long ? std::min(max_seq_len, long_threshold(t, batch)) : max_seq_len;
+        int shape = longest <= kStreamMaxLen ? t.single_block_kernel : 1;
+        const bool auto_fit = shape == 0 && !classic_knobs && longest > 16384 && batch >= t.wide_batch_min;
         if (auto_fit) shape = 2;
         if (shape >= 2) {
             sc = stream_config(shape, k, t);

@@ -1,6 +1,6 @@
 """GPU parity of the warp-specialised single-block kernel (8 streaming warps,
-4 resolving warps, two candidate-buffer / histogram sets) against the CPU
-oracle: the kernel forced (`single_block_kernel = 2`) over the score
+4 or 8 resolving warps, two candidate-buffer / histogram sets; rows of up to
+65536) against the CPU oracle: the kernel forced (`single_block_kernel = 2`) over the score
 distributions, k boundaries, special values and ragged tails, every fallback
 of the resolving warps (a gate too tight or too loose, no gate, the
 histogram-only first pass, buffer overflow), batches whose rows span several
@@ -34,7 +34,7 @@ def _make(scores, lens, k, page_size=1):
 @pytest.mark.parametrize("k", [1, 37, 512, 640, 2048])
 @pytest.mark.parametrize("shape", SHAPES)
 def test_stream_random_ragged(dist, k, shape):
-    wl = workloads.random_case(seed=900 + DISTS.index(dist) * 1000 + k, batch=40, min_len=0, max_len=90001, k=k,
+    wl = workloads.random_case(seed=900 + DISTS.index(dist) * 1000 + k, batch=40, min_len=0, max_len=65536, k=k,
                                page_size=64, dist=dist)
     with tuning(**single(shape)):
         out, raw, flags = run_gpu(wl)
@@ -54,7 +54,7 @@ def test_stream_fallbacks(mode, shape):
              "small_cap": dict(candidate_capacity=2048)}[mode]
     for dist in ("normal", "bf16", "flat", "neginf"):
         wl = workloads.random_case(seed=950 + len(mode) * 7 + DISTS.index(dist), batch=24, min_len=0,
-                                   max_len=200001, k=512, page_size=32, dist=dist)
+                                   max_len=65536, k=512, page_size=32, dist=dist)
         with tuning(**single(shape), **extra):
             out, raw, flags = run_gpu(wl)
         compare(wl, out, raw)
@@ -97,7 +97,7 @@ def test_stream_ties_across_the_threshold(shape):
     """Many copies of the k-th value: the smallest positions among them, from
     the buffer (position rounds) and from re-reads (the ordered final pass)."""
     rng = np.random.default_rng(970)
-    S = 70000
+    S = 65536
     rows = []
     for frac in (0.002, 0.02, 0.2, 0.6):
         r = rng.standard_normal(S).astype(np.float32)
@@ -159,8 +159,8 @@ def test_stream_with_cluster_launch(shape):
     from sparse_attention_indexer_uint32_gb300 import _lib
 
     wl = workloads.random_case(seed=996, batch=600, min_len=100, max_len=300000, k=512, page_size=64, dist="bf16")
-    assert _lib.topk_transform_launches(wl.batch, wl.max_seq_len, wl.k) == 2
-    with tuning(single_block_kernel=shape):
+    with tuning(single_block_kernel=shape, long_threshold_large_batch=65536):
+        assert _lib.topk_transform_launches(wl.batch, wl.max_seq_len, wl.k) == 2
         out, raw, flags = run_gpu(wl)
     compare(wl, out, raw)
     assert flags == 0
