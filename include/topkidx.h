@@ -265,8 +265,8 @@ typedef struct {
                                            wide_batch_min rows on, when two blocks fit on an SM);
                                            1: the single-role kernel; 2 / 3: the warp-specialised
                                            kernel, in which 8 warps stream row q while other warps
-                                           finish row q - 1: 2 = 4 finishing warps, a 2 x 28 KB
-                                           ring, two blocks per SM (k <= 640); 3 = 8 finishing
+                                           finish row q - 1: 2 = 4 finishing warps, a 2 x 32 KB
+                                           ring, two blocks per SM (k <= 624); 3 = 8 finishing
                                            warps, up to 4 x 32 KB, one block per SM.  It takes
                                            rows of up to 65536; longer ones use the single-role
                                            kernel whatever this field says                       */

@@ -162,7 +162,7 @@ __host__ __device__ inline Layout make_layout(int cluster, int tile, int stages,
 // and compute the gate of row q + 1, with two candidate-buffer / histogram
 // sets.
 constexpr int kStreamWarps = 8;
-constexpr int kStreamItemsMax = 64;     // work items per window of the warp-specialised kernel
+constexpr int kStreamItemsMax = 32;     // work items per window of the warp-specialised kernel
 constexpr int32_t kStreamMaxLen = 65536;  // longest row it takes (16-bit candidate positions)
 
 struct __align__(16) SetControl {

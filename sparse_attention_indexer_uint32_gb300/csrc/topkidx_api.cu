@@ -207,10 +207,10 @@ topk_status_t resident_warp_units(int* units) {
 }
 
 // Launch shapes of the warp-specialised single-block kernel.  Two candidate
-// buffers of max(2560, 4k) entries (shape 2) or max(3072, 4k) (shape 3), of
+// buffers of max(2496, 4k) entries (shape 2) or max(3072, 4k) (shape 3), of
 // 6 bytes each (rows of up to 65536).
-//  - shape 2: 4 resolving warps, 28 KB copies in a two-stage ring: about
-//    106 KB of shared memory at k <= 640, two blocks per SM;
+//  - shape 2: 4 resolving warps, 32 KB copies in a two-stage ring: about
+//    112.5 KB of shared memory at k <= 624, two blocks per SM;
 //  - shape 3: 8 resolving warps, 32 KB copies in a ring as deep as the
 //    shared memory allows (up to four stages), one block per SM.
 struct StreamConfig {
@@ -222,10 +222,10 @@ struct StreamConfig {
 StreamConfig stream_config(int shape, int32_t k, const topk_tuning_t& t) {
     StreamConfig c;
     c.resolve_warps = shape == 3 ? 8 : 4;
-    c.tile = shape == 3 ? 8192 : 7168;
+    c.tile = 8192;
     int cap = t.candidate_capacity;
     if (cap == 0) {
-        cap = std::max(shape == 3 ? 3072 : 2560, 4 * k);
+        cap = std::max(shape == 3 ? 3072 : 2496, 4 * k);
         if (cap > 16384) cap = 16384;
         cap = (cap + 63) / 64 * 64;
     }
