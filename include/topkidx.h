@@ -254,7 +254,7 @@ typedef struct {
                                            never drops a top-k element); other kernels ignore it  */
     int32_t warp_rows;                  /* the warp-per-row kernel (one warp per row) for batches
                                            whose rows are all at most 16384 long, with k <= 512:
-                                           0: automatic (from wide_batch_min rows on); 1: always;
+                                           0: automatic (from warp_batch_min rows on); 1: always;
                                            2: never                                              */
     int32_t wait_limit_us;              /* 0: 2 s; else 1..60000000: how long a select block waits
                                            for one bulk copy of scores before it gives up, sets
@@ -262,7 +262,7 @@ typedef struct {
                                            stops issuing copies; the call still returns, and the
                                            block waits for its copies in flight before it exits  */
     int32_t single_block_kernel;        /* 0: automatic (shape 2 for rows of 16K..64K from
-                                           wide_batch_min rows on, when two blocks fit on an SM);
+                                           stream_batch_min rows on, when two blocks fit an SM);
                                            1: the single-role kernel; 2 / 3: the warp-specialised
                                            kernel, in which 8 warps stream row q while other warps
                                            finish row q - 1: 2 = 4 finishing warps, a 2 x 32 KB
@@ -273,8 +273,10 @@ typedef struct {
     int32_t long_threshold_large_batch; /* long row if seq_len > this, batch > large_batch_min
                                            (131072)                                              */
     int32_t large_batch_min;            /* (64)                                                  */
-    int32_t wide_batch_min;             /* batch from which the automatic dispatch takes the
-                                           warp-per-row and warp-specialised kernels (1024)      */
+    int32_t warp_batch_min;             /* batch from which the automatic dispatch takes the
+                                           warp-per-row kernel (1024)                            */
+    int32_t stream_batch_min;           /* batch from which the automatic dispatch takes the
+                                           warp-specialised kernel (384)                         */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

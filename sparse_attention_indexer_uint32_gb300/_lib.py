@@ -73,7 +73,8 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("single_block_kernel", ctypes.c_int32),
         ("long_threshold_large_batch", ctypes.c_int32),
         ("large_batch_min", ctypes.c_int32),
-        ("wide_batch_min", ctypes.c_int32),
+        ("warp_batch_min", ctypes.c_int32),
+        ("stream_batch_min", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

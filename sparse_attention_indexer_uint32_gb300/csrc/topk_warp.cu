@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
 #pragma unroll
                 for (int q = 0; q < kWVec; ++q) {
                     const uint32_t v = step * kWStep + static_cast<uint32_t>(q * 32 + lane);
-                    x[q] = v < nvec ? __ldg(row4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[q] = v < nvec ? __ldcs(row4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             };
             auto test = [&](const float4* x, uint32_t step) {
@@ -354,6 +354,25 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                 if (step + 1u < nsteps) test(xb, step + 1u);
             }
             __syncwarp();
+            {
+                // The warp's next row: its gate samples into L2 now (one 128-byte
+                // segment per lane), so that its gate does not wait on DRAM behind
+                // the stream; the row streams above use evict-first loads, which
+                // leave these lines (and the page-table lines) in L2.
+                const int32_t itn = it + nwarps;
+                if (itn < n_items) {
+                    const int32_t rown =
+                        identity ? (itn < n_first ? itn : itn - n_first)
+                                 : (itn < n_first ? (p.items ? p.items[itn] : itn) : p.items2[itn - n_first]);
+                    if (rown >= 0 && rown < p.batch) {
+                        const int32_t Ln = min(max(p.seq_lens[rown], 0), p.max_seq_len);
+                        const uint32_t Mn = min(static_cast<uint32_t>(kWSamples), static_cast<uint32_t>(Ln));
+                        if (Ln > p.k && 32u * static_cast<uint32_t>(lane) < Mn)
+                            ptx::prefetch_l2(p.scores + static_cast<int64_t>(rown) * p.row_stride +
+                                             wsegment(static_cast<uint32_t>(lane), static_cast<uint32_t>(Ln), Mn));
+                    }
+                }
+            }
             if (wcnt <= kWarpCap) {
                 // Key the buffered elements.  An element that passed the float
                 // compare but whose key is below the gate can only be a NaN; it

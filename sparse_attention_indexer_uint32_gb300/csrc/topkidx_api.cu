@@ -41,9 +41,9 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // with the seq-dependent cap of the same PR expressed as a third tier: at
 // batch 128 x 128K one block per row is 1.3-1.8x faster than clusters, at
 // 256K clusters win at every batch.  From 1024 rows on, short rows (<= 16K,
-// k <= 512) go to the warp-per-row kernel and mid rows (<= 64K, k <= 640) to
-// the warp-specialised kernel (1.1-1.6x on those shapes).
-topk_tuning_t g_tuning = {16384, 65536, 16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 131072, 64, 1024};
+// k <= 512) go to the warp-per-row kernel (1.2-1.6x), and from 384 rows on,
+// mid rows (16K..64K, k <= 624) to the warp-specialised kernel (1.05-1.2x).
+topk_tuning_t g_tuning = {16384, 65536, 16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 131072, 64, 1024, 384};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -350,7 +350,8 @@ topk_status_t topk_get_tuning(topk_tuning_t* tuning_host) {
 topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (!t) return TOPK_EINVAL;
     if (t->long_threshold_small_batch < 0 || t->long_threshold < 0 || t->small_batch_max < 0 ||
-        t->long_threshold_large_batch < 0 || t->large_batch_min < 0 || t->wide_batch_min < 0)
+        t->long_threshold_large_batch < 0 || t->large_batch_min < 0 || t->warp_batch_min < 0 ||
+        t->stream_batch_min < 0)
         return TOPK_EINVAL;
     if (t->cluster_size != 0 && t->cluster_size != 2 && t->cluster_size != 4 && t->cluster_size != 8 &&
         t->cluster_size != 16)
@@ -447,7 +448,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     // takes every row.
     const bool warp_fits = !launch_long && !fold_short && max_seq_len <= static_cast<int32_t>(kWarpMaxLen) &&
                            k <= kWarpMaxK;
-    const bool warp_ok = warp_fits && (t.warp_rows == 1 || (t.warp_rows == 0 && batch >= t.wide_batch_min));
+    const bool warp_ok = warp_fits && (t.warp_rows == 1 || (t.warp_rows == 0 && batch >= t.warp_batch_min));
     if (warp_ok) {
         int warp_units = 0;
         {
@@ -480,7 +481,7 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         // kernel keeps 16-bit positions, so it takes rows of up to 65536.
         const int32_t longest = launch_long ? std::min(max_seq_len, long_threshold(t, batch)) : max_seq_len;
         int shape = longest <= kStreamMaxLen ? t.single_block_kernel : 1;
-        const bool auto_fit = shape == 0 && !classic_knobs && longest > 16384 && batch >= t.wide_batch_min;
+        const bool auto_fit = shape == 0 && !classic_knobs && longest > 16384 && batch >= t.stream_batch_min;
         if (auto_fit) shape = 2;
         if (shape >= 2) {
             sc = stream_config(shape, k, t);

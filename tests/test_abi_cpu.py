@@ -76,7 +76,7 @@ def test_tuning_roundtrip_and_validation(lib):
                            ("single_block_threads", 128), ("single_block_copy_bytes", 4096), ("single_block_stages", 1),
                            ("single_block_stages", 9), ("gate_refresh_tiles", -1), ("gate_refresh_tiles", 65),
                            ("warp_rows", 3), ("warp_rows", -1), ("long_threshold_large_batch", -1),
-                           ("large_batch_min", -1), ("wide_batch_min", -1), ("wait_limit_us", -1),
+                           ("large_batch_min", -1), ("warp_batch_min", -1), ("stream_batch_min", -1), ("wait_limit_us", -1),
                            ("wait_limit_us", 60000001), ("single_block_kernel", -1), ("single_block_kernel", 4)):
             t2 = lib.topk_tuning_t(**old.as_dict())
             setattr(t2, field, bad)
