@@ -62,7 +62,10 @@ typedef enum {
  * Bytes of device workspace that topk_plan needs for `batch` rows (the plan's
  * work lists, after SGLang PR #26788, commit "Replace the per-element cluster
  * launch ... with a FIXED persistent pool": a compacted list of long items,
- * plus a list of the other rows and a flag word).  Returns 0 for batch < 1.
+ * plus a list of the other rows and a flag word; then the state and the
+ * candidate buffers of the opt-in segment-split path for the first 128 rows,
+ * 64 KB per row plus 70 KB: about 8.5 MB from 128 rows on).  Returns 0 for
+ * batch < 1.
  */
 size_t topk_plan_workspace_bytes(int32_t batch);
 
@@ -178,7 +181,8 @@ topk_status_t topk_read_flags(void* workspace, uint32_t* flags_host, int32_t cle
  * must not call cudaMalloc behind its allocator's back -- this call keeps the
  * plan's work lists in a fixed device array owned by the library instead of
  * a caller workspace.  Every GPU that loads the library holds that array
- * (about 128 KiB) until the process exits.  Arguments and outputs are those
+ * (topk_plan_workspace_bytes(TOPK_NOALLOC_MAX_BATCH), about 8.6 MB) until the
+ * process exits.  Arguments and outputs are those
  * of topk_transform; the caller still passes scores, seq_lens, the page table
  * and the output buffers.
  *
@@ -277,6 +281,18 @@ typedef struct {
                                            warp-per-row kernel (1024)                            */
     int32_t stream_batch_min;           /* batch from which the automatic dispatch takes the
                                            warp-specialised kernel (384)                         */
+    int32_t split_rows;                 /* the segment-split path (the rows of the whole batch
+                                           cut into segments that every SM streams; the block
+                                           that finishes a row's last segment resolves it), for
+                                           batches of up to 128 rows: 1: always; 0 (automatic)
+                                           and 2: never -- on GB300 the cluster kernel was faster
+                                           on every long-row shape timed                         */
+    int32_t split_segment;              /* 0: automatic; else a power of two, 4096..1048576:
+                                           elements per segment of the split path (raised where
+                                           the batch would need more than 16384 segments)        */
+    int32_t split_full_resolve;         /* 1: the split path resolves every row from a full
+                                           re-read of the row (the path it otherwise takes only
+                                           when a row's gate misses); for tests                  */
 } topk_tuning_t;
 
 topk_status_t topk_get_tuning(topk_tuning_t* tuning_host);

@@ -75,6 +75,9 @@ class topk_tuning_t(ctypes.Structure):  # noqa: N801 - C name
         ("large_batch_min", ctypes.c_int32),
         ("warp_batch_min", ctypes.c_int32),
         ("stream_batch_min", ctypes.c_int32),
+        ("split_rows", ctypes.c_int32),
+        ("split_segment", ctypes.c_int32),
+        ("split_full_resolve", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

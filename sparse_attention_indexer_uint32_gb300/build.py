@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libtopkidx.so")
-SOURCES = ["topk_kernels.cu", "topk_stream.cu", "topk_warp.cu", "topkidx_api.cu", "topk_noalloc.cu"]
+SOURCES = ["topk_kernels.cu", "topk_stream.cu", "topk_warp.cu", "topk_split.cu", "topkidx_api.cu", "topk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

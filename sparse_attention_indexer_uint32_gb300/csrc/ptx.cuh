@@ -32,6 +32,20 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Asks the bulk-copy engine to bring `bytes` bytes at `p` into L2 (address
+// 16-byte aligned, size a multiple of 16): one instruction, no completion to
+// wait for.  The range must lie inside an allocation.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// max of two floats that is a NaN when either input is one (max.NaN).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 // ------------------------------------------------- shared-memory accessors
 // Explicit .shared accesses on 32-bit shared-window addresses, so that hot
 // loops never fall back to generic loads, stores or atomics.  All carry a

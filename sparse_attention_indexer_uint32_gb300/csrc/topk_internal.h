@@ -48,10 +48,75 @@ struct PlanHeader {
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
-inline size_t plan_bytes(int32_t batch) {
-    if (batch < 1) return 0;
-    size_t b = sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(batch);
-    return (b + 255) / 256 * 256;
+// The segment-split path (topk_split.cu): a batch of up to kSplitMaxRows
+// rows is cut into segments that a persistent grid streams; each row's gated
+// candidates are collected in the workspace, and the block that finishes a
+// row's last segment resolves the row.
+constexpr int32_t kSplitMaxRows = 128;     // rows of one split launch (the whole batch)
+constexpr uint32_t kSplitCap = 8192;       // candidate entries per row (64-bit composites)
+constexpr int32_t kSplitMaxUnits = 16384;  // segments of one launch
+constexpr int kSplitThreads = 512;         // threads per block of the streaming kernel
+constexpr int kSplitGateThreads = 512;     // threads per block of the gate kernel (one row each)
+constexpr int kSplitMaxSamples = 8192;     // gate samples per row
+
+// Per-row state of the split path, rewritten by the gate kernel every call.
+struct SplitRow {
+    uint32_t lo;      // gate key: elements with key > lo are candidates, key == lo are counted
+    uint32_t n_gt;    // candidates reserved (may run past kSplitCap: overflow)
+    uint32_t n_eq;    // elements with key == lo
+    uint32_t done;    // segments finished
+    int32_t len;      // clamped seq_len
+    int32_t nunits;   // segments of the row (0: the gate kernel wrote the row)
+    int32_t pad[2];
+};
+static_assert(sizeof(SplitRow) == 32, "split row state is 32 bytes");
+struct SplitHeader {
+    uint32_t next_unit;    // segments handed out so far
+    uint32_t total_units;  // segments of the launch
+    uint32_t pad[14];
+};
+static_assert(sizeof(SplitHeader) == 64, "split header is 64 bytes");
+
+__host__ __device__ constexpr size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+__host__ __device__ constexpr int32_t split_rows_of(int32_t batch) {
+    return batch < kSplitMaxRows ? batch : kSplitMaxRows;
+}
+// The plan's own part: header + the two row lists.
+__host__ __device__ constexpr size_t plan_core_bytes(int32_t batch) {
+    return round256(sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(batch));
+}
+// The split path's fixed part (header, row states, segment starts, per-segment
+// tie counts), then kSplitCap candidates per row.
+__host__ __device__ constexpr size_t split_fixed_bytes(int32_t rows) {
+    return round256(sizeof(SplitHeader) + sizeof(SplitRow) * static_cast<size_t>(rows) +
+                    sizeof(int32_t) * static_cast<size_t>(rows + 1) +
+                    sizeof(uint32_t) * static_cast<size_t>(kSplitMaxUnits));
+}
+__host__ __device__ constexpr size_t split_bytes(int32_t batch) {
+    return split_fixed_bytes(split_rows_of(batch)) +
+           sizeof(uint64_t) * static_cast<size_t>(kSplitCap) * static_cast<size_t>(split_rows_of(batch));
+}
+__host__ __device__ constexpr size_t plan_bytes(int32_t batch) {
+    return batch < 1 ? 0 : plan_core_bytes(batch) + split_bytes(batch);
+}
+struct SplitRegion {
+    SplitHeader* hdr;
+    SplitRow* rows;
+    int32_t* unit_start;  // [rows + 1]: first segment of each row, then the total
+    uint32_t* unit_ties;  // [kSplitMaxUnits]: elements with key == lo per segment
+    uint64_t* cand;       // [rows][kSplitCap]: (key << 32) | ~position
+};
+__host__ __device__ inline SplitRegion split_region(void* ws, int32_t batch) {
+    const int32_t rows = split_rows_of(batch);
+    char* b = static_cast<char*>(ws) + plan_core_bytes(batch);
+    SplitRegion r;
+    r.hdr = reinterpret_cast<SplitHeader*>(b);
+    r.rows = reinterpret_cast<SplitRow*>(b + sizeof(SplitHeader));
+    r.unit_start = reinterpret_cast<int32_t*>(b + sizeof(SplitHeader) + sizeof(SplitRow) * rows);
+    r.unit_ties = reinterpret_cast<uint32_t*>(b + sizeof(SplitHeader) + sizeof(SplitRow) * rows +
+                                              sizeof(int32_t) * (rows + 1));
+    r.cand = reinterpret_cast<uint64_t*>(b + split_fixed_bytes(rows));
+    return r;
 }
 __host__ __device__ inline int32_t* plan_long_list(void* ws) {
     return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + sizeof(PlanHeader));
@@ -89,6 +154,28 @@ struct SelectParams {
     int32_t force_two_pass;
     int32_t disable_gate;
     uint64_t timeout_ns;
+};
+
+// Parameters of the two kernels of the segment-split path.
+struct SplitParams {
+    const float* scores;
+    int64_t row_stride;
+    const int32_t* seq_lens;
+    int32_t batch;            // <= kSplitMaxRows; rows 0..batch-1 in order
+    int32_t max_seq_len;
+    const int32_t* page_table;
+    int64_t pt_stride;
+    int32_t log2_page;
+    int32_t k;
+    int32_t* out;
+    int32_t* raw_out;
+    const PlanHeader* plan;
+    uint32_t* flags;
+    SplitRegion ws;
+    int32_t seg;              // elements per segment: a power of two, 4096..1048576
+    int32_t samples;          // gate samples per row, <= kSplitMaxSamples
+    int32_t full_resolve;     // 1: every row is resolved by the full-row path (tests)
+    int32_t disable_gate;     // 1: gate key 0 (every element is a candidate)
 };
 
 struct __align__(16) Control {
@@ -239,5 +326,9 @@ cudaError_t launch_stream_select(const SelectParams& p, int resolve_warps, int g
 cudaError_t stream_select_occupancy(int resolve_warps, size_t smem, int* units_out);
 cudaError_t warp_select_occupancy(int* units_out);
 size_t warp_select_smem_bytes();
+// The segment-split path (topk_split.cu): the gate kernel (one block per
+// row), then the persistent streaming kernel on `grid` blocks.
+cudaError_t launch_split(const SplitParams& p, int grid, cudaStream_t stream);
+cudaError_t split_occupancy(int* blocks_out);
 
 }  // namespace topkidx

@@ -21,10 +21,11 @@ namespace topkidx {
 namespace {
 
 constexpr int32_t kNoAllocMaxBatch = TOPK_NOALLOC_MAX_BATCH;
-constexpr size_t kNoAllocWorkspaceBytes =
-    (sizeof(PlanHeader) + 2 * sizeof(int32_t) * static_cast<size_t>(kNoAllocMaxBatch) + 255) / 256 * 256;
+constexpr size_t kNoAllocWorkspaceBytes = plan_bytes(kNoAllocMaxBatch);
 
-// The shared scratch: one plan workspace for up to kNoAllocMaxBatch rows.
+// The shared scratch: one plan workspace for up to kNoAllocMaxBatch rows
+// (the plan's lists, and the segment-split path's candidate buffers for its
+// first kSplitMaxRows rows: about 8.6 MB).
 // In host code this name is only a stand-in for the device symbol; its
 // device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];

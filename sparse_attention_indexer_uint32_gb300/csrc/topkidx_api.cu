@@ -43,7 +43,7 @@ topk_status_t cuda_fail(cudaError_t e, const char* where) {
 // 256K clusters win at every batch.  From 1024 rows on, short rows (<= 16K,
 // k <= 512) go to the warp-per-row kernel (1.2-1.6x), and from 384 rows on,
 // mid rows (16K..64K, k <= 624) to the warp-specialised kernel (1.05-1.2x).
-topk_tuning_t g_tuning = {16384, 65536, 16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 131072, 64, 1024, 384};
+topk_tuning_t g_tuning = {16384, 65536, 16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 131072, 64, 1024, 384, 0, 0, 0};
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -180,6 +180,49 @@ topk_status_t resident_units(int cluster, int threads, size_t smem, int* units) 
     return TOPK_OK;
 }
 
+// Resident blocks of the segment-split streaming kernel on the current device.
+topk_status_t resident_split_units(int* units) {
+    static std::map<int, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = cache.find(dev);
+        if (it != cache.end()) {
+            *units = it->second;
+            return TOPK_OK;
+        }
+    }
+    int u = 0;
+    const cudaError_t e = split_occupancy(&u);
+    if (e != cudaSuccess) return cuda_fail(e, "split select occupancy query");
+    if (u <= 0) {
+        snprintf(g_last_error, sizeof(g_last_error), "split select kernel cannot be resident");
+        return TOPK_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    cache[dev] = u;
+    *units = u;
+    return TOPK_OK;
+}
+
+// Elements per segment of the split path: about four segments per resident
+// block over the batch's upper bound of elements (batch x max_seq_len),
+// 4096..32768, doubled while the segment list would not fit; 0 when no size
+// up to 1M elements fits.
+int32_t split_segment(int32_t batch, int32_t max_seq_len, const topk_tuning_t& t, int units) {
+    int64_t seg = t.split_segment;
+    if (seg == 0) {
+        const int64_t est = static_cast<int64_t>(batch) * max_seq_len / (4 * static_cast<int64_t>(units));
+        seg = 4096;
+        while (seg < est && seg < 32768) seg <<= 1;
+    }
+    while (static_cast<int64_t>(batch) * ((static_cast<int64_t>(max_seq_len) + seg - 1) / seg) > kSplitMaxUnits &&
+           seg <= (1 << 20))
+        seg <<= 1;
+    return seg <= (1 << 20) ? static_cast<int32_t>(seg) : 0;
+}
+
 // Resident blocks of the warp-per-row kernel on the current device.
 topk_status_t resident_warp_units(int* units) {
     static std::map<int, int> cache;
@@ -292,11 +335,29 @@ struct Dispatch {
     bool fold_short = false;
     PathConfig cl = {};
     int cl_units = 0;
+    bool split = false;   // the segment-split path takes the whole batch
+    int32_t split_seg = 0;
+    int split_units = 0;
 };
 
 topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, const topk_tuning_t& t, Dispatch* d) {
     *d = Dispatch();
     d->launch_long = max_seq_len > long_threshold(t, batch);
+    // The segment-split path, when asked for and the batch fits one split
+    // launch.  The automatic dispatch does not take it: on GB300 the cluster
+    // kernel was faster on every long-row shape timed (1 / 8 / 32 x 1M,
+    // k = 2048; 128 ragged rows up to 256K, k = 1024), because each segment
+    // ends in a block barrier and a fenced count, and the gate is a kernel of
+    // its own.
+    if (batch <= kSplitMaxRows && t.split_rows == 1) {
+        const topk_status_t r = resident_split_units(&d->split_units);
+        if (r != TOPK_OK) return r;
+        d->split_seg = split_segment(batch, max_seq_len, t, d->split_units);
+        if (d->split_seg > 0) {
+            d->split = true;
+            return TOPK_OK;
+        }
+    }
     if (!d->launch_long) return TOPK_OK;
     int cluster = t.cluster_size;
     if (cluster == 0) {
@@ -373,6 +434,11 @@ topk_status_t topk_set_tuning(const topk_tuning_t* t) {
     if (t->warp_rows < 0 || t->warp_rows > 2) return TOPK_EINVAL;
     if (t->wait_limit_us < 0 || t->wait_limit_us > 60000000) return TOPK_EINVAL;
     if (t->single_block_kernel < 0 || t->single_block_kernel > 3) return TOPK_EINVAL;
+    if (t->split_rows < 0 || t->split_rows > 2) return TOPK_EINVAL;
+    if (t->split_segment != 0 && (!is_pow2(t->split_segment) || t->split_segment < 4096 ||
+                                  t->split_segment > (1 << 20)))
+        return TOPK_EINVAL;
+    if (t->split_full_resolve < 0 || t->split_full_resolve > 1) return TOPK_EINVAL;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_tuning = *t;
     return TOPK_OK;
@@ -439,6 +505,30 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
     {
         const topk_status_t r = decide_dispatch(batch, max_seq_len, k, t, &d);
         if (r != TOPK_OK) return r;
+    }
+    if (d.split) {
+        SplitParams q = {};
+        q.scores = scores;
+        q.row_stride = row_stride;
+        q.seq_lens = seq_lens;
+        q.batch = batch;
+        q.max_seq_len = max_seq_len;
+        q.page_table = page_table;
+        q.pt_stride = page_table_stride;
+        q.log2_page = p.log2_page;
+        q.k = k;
+        q.out = out_indices;
+        q.raw_out = out_raw_indices_or_null;
+        q.plan = hdr;
+        q.flags = &hdr->flags;
+        q.ws = split_region(workspace, batch);
+        q.seg = d.split_seg;
+        q.samples = t.samples > 0 ? t.samples : kSplitMaxSamples;
+        q.full_resolve = t.split_full_resolve;
+        q.disable_gate = t.disable_gate;
+        const cudaError_t e = launch_split(q, d.split_units, st);
+        if (e != cudaSuccess) return cuda_fail(e, "split select launch");
+        return TOPK_OK;
     }
     const bool launch_long = d.launch_long;
     const bool fold_short = d.fold_short;
@@ -567,6 +657,7 @@ int32_t topk_transform_launches(int32_t batch, int32_t max_seq_len, int32_t k) {
     Dispatch d;
     const topk_status_t r = decide_dispatch(batch, max_seq_len, k, t, &d);
     if (r != TOPK_OK) return r;
+    if (d.split) return 2;  // the gate kernel and the streaming kernel
     return (d.fold_short ? 0 : 1) + (d.launch_long ? 1 : 0);
 }
 

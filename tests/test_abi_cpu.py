@@ -120,7 +120,7 @@ def test_host_side_argument_checks_return_before_any_launch(lib):
     assert c.topk_plan(fake, 0, 10, fake, 4096, None) == lib.TOPK_EINVAL
     assert c.topk_plan(fake, 4, -1, fake, 4096, None) == lib.TOPK_EINVAL
     assert c.topk_plan(fake, 1000, 10, fake, 64, None) == lib.TOPK_ENOSPACE
-    assert c.topk_plan(fake, 4, 10, fake + 4, 4096, None) == lib.TOPK_EALIGN
+    assert c.topk_plan(fake, 4, 10, fake + 4, lib.topk_plan_workspace_bytes(4), None) == lib.TOPK_EALIGN
     # page transform / key map
     assert c.topk_page_transform(fake, 0, 4, fake, 1, 64, fake, None) == lib.TOPK_EINVAL
     assert c.topk_page_transform(fake, 2, 4, fake, 1, 63, fake, None) == lib.TOPK_EINVAL

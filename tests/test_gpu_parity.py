@@ -100,7 +100,7 @@ def test_random_ragged_single_block(dist, k):
 def test_cluster_path_forced(cluster, dist, batch):
     wl = workloads.random_case(seed=100 + cluster + batch, batch=batch, min_len=1, max_len=70001, k=700,
                                page_size=16, dist=dist)
-    with tuning(long_threshold=0, long_threshold_small_batch=0, cluster_size=cluster):
+    with tuning(long_threshold=0, long_threshold_small_batch=0, cluster_size=cluster, split_rows=2):
         out, raw, _ = run_gpu(wl)
     compare(wl, out, raw)
 
@@ -111,7 +111,7 @@ def test_two_pass_streaming_forced(cluster, dist):
     wl = workloads.random_case(seed=200 + cluster, batch=10, min_len=3000, max_len=90000, k=300, page_size=32,
                                dist=dist)
     thr = 0 if cluster > 1 else 1 << 30
-    with tuning(force_two_pass=1, long_threshold=thr, long_threshold_small_batch=thr):
+    with tuning(force_two_pass=1, long_threshold=thr, long_threshold_small_batch=thr, split_rows=2):
         out, raw, _ = run_gpu(wl)
     compare(wl, out, raw)
 
@@ -122,7 +122,7 @@ def test_ungated_first_pass(cluster, dist):
     wl = workloads.random_case(seed=300 + cluster, batch=9, min_len=1000, max_len=60000, k=1024, page_size=8,
                                dist=dist)
     thr = 0 if cluster > 1 else 1 << 30
-    with tuning(disable_gate=1, long_threshold=thr, long_threshold_small_batch=thr):
+    with tuning(disable_gate=1, long_threshold=thr, long_threshold_small_batch=thr, split_rows=2):
         out, raw, _ = run_gpu(wl)
     compare(wl, out, raw)
 
@@ -133,9 +133,11 @@ def test_few_samples_gate_misses(samples):
     fallbacks must still give the exact answer."""
     wl = workloads.random_case(seed=400 + samples, batch=16, min_len=5000, max_len=40000, k=2048, page_size=64,
                                dist="normal")
-    with tuning(samples=samples):
-        out, raw, _ = run_gpu(wl)
-    compare(wl, out, raw)
+    for split_rows in (2, 1):  # the cluster kernel, then the segment-split path
+        with tuning(samples=samples, split_rows=split_rows):
+            out, raw, flags = run_gpu(wl)
+        compare(wl, out, raw)
+        assert flags == 0
 
 
 @pytest.mark.parametrize("fill", [1, 100])
@@ -147,7 +149,7 @@ def test_gate_fill_extremes(fill, cluster):
     wl = workloads.random_case(seed=450 + fill + cluster, batch=24, min_len=3000, max_len=200000, k=512,
                                page_size=64, dist="bf16")
     thr = 0 if cluster > 1 else 1 << 30
-    with tuning(gate_fill_percent=fill, long_threshold=thr, long_threshold_small_batch=thr):
+    with tuning(gate_fill_percent=fill, long_threshold=thr, long_threshold_small_batch=thr, split_rows=2):
         out, raw, _ = run_gpu(wl)
     compare(wl, out, raw)
 
@@ -208,9 +210,10 @@ def test_gate_refresh_modes(mode):
 def test_trend_rows_cluster():
     """Rows with a positional trend (the gate's sample must not alias)."""
     wl = workloads.long_context(batch=2, seq_len=300000)
-    with tuning(long_threshold=0, long_threshold_small_batch=0):
-        out, raw, _ = run_gpu(wl)
-    compare(wl, out, raw)
+    for split_rows in (2, 1):  # the cluster kernel, then the segment-split path
+        with tuning(long_threshold=0, long_threshold_small_batch=0, split_rows=split_rows):
+            out, raw, _ = run_gpu(wl)
+        compare(wl, out, raw)
 
 
 # ------------------------------------------------------------------ edge cases
