@@ -90,19 +90,35 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name: str):
-    """DRAM bytes per launch of the select kernel from the committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
+def _profile_summary(workload_name: str):
+    """The committed ncu summary of the workload's select kernel, if it was
+    taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", f"select_kernel_{workload_name}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != source_digest():
+    if not m_sha or m_sha.group(1) != source_digest():
         return None
-    return int(m_tr.group(1))
+    return text
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the select kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    text = _profile_summary(workload_name)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text) if text else None
+    return int(m_tr.group(1)) if m_tr else None
+
+
+def profiled_kernel(workload_name: str) -> str:
+    """The select kernel the dispatch launches for the workload, as the
+    committed ncu summary names it (its title), when that summary is current."""
+    text = _profile_summary(workload_name)
+    m = re.match(r"#\s*`([^`]+)`", text) if text else None
+    name = m.group(1) if m else "the select kernel(s) of topk_transform"
+    return f"{name}; events around the topk_transform call"
 
 
 class ClockSampler:
@@ -529,7 +545,7 @@ def gpu_line(name: str, steps: int, warmup: int, world: int, rank: int, local: i
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(name),
                      "frac_of_spec": round(achieved / SPEC_HBM_GBS, 4), "spec_peak": SPEC_HBM_GBS,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                     "kernel": "select_kernel (topk_transform), events around the call"},
+                     "kernel": profiled_kernel(name)},
     }
     if full and not quick:
         e2e_steps = max(3, min(steps, 10))
