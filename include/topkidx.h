@@ -232,8 +232,9 @@ typedef struct {
                                            (65536)                                               */
     int32_t small_batch_max;            /* (16)                                                  */
     int32_t cluster_size;               /* blocks per long row: 2, 4, 8 or 16; 0: automatic (16
-                                           for up to 4 rows, 8 while every row gets a resident
-                                           8-block cluster, else 4)                              */
+                                           for up to 4 rows; else 4 for rows of at most 64K; else
+                                           8 while every row gets a resident 8-block cluster,
+                                           else 4)                                               */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every
                                            row takes the two-pass streaming path                  */
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */

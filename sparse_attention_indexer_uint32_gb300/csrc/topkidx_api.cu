@@ -361,11 +361,16 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
     if (!d->launch_long) return TOPK_OK;
     int cluster = t.cluster_size;
     if (cluster == 0) {
-        // 16 blocks per row for up to 4 rows, 8 while every row gets a resident
+        // 16 blocks per row for up to 4 rows; then 4 for rows of at most 64K
+        // (8 blocks would give each block 8K elements or fewer: 16 x 64K takes
+        // 25.3 us with 8-block clusters and 21.5 us with 4-block ones, and 4 is
+        // no slower at 4 or 8 rows); else 8 while every row gets a resident
         // 8-block cluster at once, else 4 (the sweep: 8 beats 16 from 8 rows
         // on, 4 beats 8 once the rows exceed one wave of 8-block clusters).
         if (batch <= 4 && static_cast<int64_t>(batch) * 16 <= sm_count()) {
             cluster = 16;
+        } else if (max_seq_len <= 65536) {
+            cluster = 4;
         } else {
             const PathConfig c8 = path_config(8, k, batch, max_seq_len, t);
             int u8 = 0;
