@@ -341,3 +341,25 @@ def test_mixed_batch_with_long_and_short_launches():
     compare(wl, out, raw)
     check_properties_all_rows(wl, raw)
     assert flags == 0
+
+
+@pytest.mark.parametrize("path", ["auto", "single_block", "split"])
+def test_rows_far_past_one_million(path):
+    """A 16M-token row, two rows of about 6M and a short one (k = 2048, a
+    permuted table): the slice, tile and position arithmetic of the cluster
+    kernel (automatic: 16 blocks per row), of one block streaming a whole
+    64 MB row, and of the segment-split path, far past the workloads' 1M."""
+    rng = np.random.default_rng(2100)
+    S = 1 << 24
+    lens = [S, 6_000_001, 6_000_000 - 3, 777]
+    scores = np.full((len(lens), S), np.inf, np.float32)
+    for b, L in enumerate(lens):
+        scores[b, :L] = rng.standard_normal(L).astype(np.float32)
+    table = workloads.permuted_table(rng, len(lens), workloads.pages_for(S, 64))
+    wl = _make(scores, lens, k=2048, page_size=64, table=table)
+    extra = {"auto": {}, "single_block": dict(long_threshold=1 << 30, long_threshold_small_batch=1 << 30),
+             "split": dict(split_rows=1)}[path]
+    with tuning(**extra):
+        out, raw, flags = run_gpu(wl)
+    compare(wl, out, raw)
+    assert flags == 0
