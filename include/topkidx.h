@@ -234,7 +234,9 @@ typedef struct {
     int32_t cluster_size;               /* blocks per long row: 2, 4, 8 or 16; 0: automatic (16
                                            for up to 4 rows; else 4 for rows of at most 64K; else
                                            8 while every row gets a resident 8-block cluster,
-                                           else 4)                                               */
+                                           else 4; then doubled while a row of max_seq_len would
+                                           fill a block's candidate buffer past 80 % at the
+                                           gate's sampling floor)                                */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every
                                            row takes the two-pass streaming path                  */
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */
@@ -286,8 +288,13 @@ typedef struct {
                                            cut into segments that every SM streams; the block
                                            that finishes a row's last segment resolves it), for
                                            batches of up to 128 rows: 1: always; 0 (automatic)
-                                           and 2: never -- on GB300 the cluster kernel was faster
-                                           on every long-row shape timed                         */
+                                           and 2: never.  On GB300 it is faster on batches that
+                                           mix a few very long rows with short ones (1 x 1M +
+                                           63 x 4K, k = 2048: 34 vs 39 us; 4 x 1M + 124 x 8K,
+                                           k = 1024: 35 vs 58 us) and slower on batches of
+                                           similar lengths (8 x 1M: 47 vs 33 us; 128 ragged rows
+                                           up to 256K: 62 vs 47 us); the host does not see the
+                                           lengths, so the caller chooses                        */
     int32_t split_segment;              /* 0: automatic; else a power of two, 4096..1048576:
                                            elements per segment of the split path (raised where
                                            the batch would need more than 16384 segments)        */

@@ -379,6 +379,22 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
             cluster = batch <= u8 ? 8 : 4;
         }
     }
+    if (t.cluster_size == 0) {
+        // At least enough blocks that a row of max_seq_len fills each block's
+        // candidate buffer to at most 80 % at the gate's sampling floor: about
+        // r_safe = E + 4 sqrt(E) + 4 of M samples are gated, E = M k / L, so a
+        // row gates about r_safe * L / M elements.  Without it, 2 x 1M rows
+        // with k = 2048 in a batch of 64 took 4-block clusters whose buffers
+        // overflowed (233 us; 40 us with 8 blocks), and a 4M row among 16 rows
+        // 8-block ones (438 us; 58 us with 16 blocks).  At 73 % (1M rows,
+        // k = 1024, 4 blocks) the buffers hold: 58 us against 67 us with 8.
+        const double L = static_cast<double>(max_seq_len);
+        const double M = static_cast<double>(t.samples > 0 && t.samples < kMaxSamples ? t.samples : kMaxSamples);
+        const double E = M * static_cast<double>(k) / L;
+        const double gated = (E + 4.0 * std::sqrt(E) + 4.0) * L / M;
+        const double cap = static_cast<double>(path_config(cluster, k, batch, max_seq_len, t).cap);
+        while (cluster < 16 && gated / cluster > 0.8 * cap) cluster *= 2;
+    }
     d->cl = path_config(cluster, k, batch, max_seq_len, t);
     const topk_status_t r = resident_units(d->cl.cluster, d->cl.threads, d->cl.smem, &d->cl_units);
     if (r != TOPK_OK) return r;

@@ -199,3 +199,24 @@ def test_split_flat_and_neginf_rows_in_the_ragged_mix():
         out, raw, flags = run_gpu(wl)
     compare(wl, out, raw)
     assert flags == 0
+
+
+@pytest.mark.parametrize("path", ["auto", "split"])
+def test_skewed_batches(path):
+    """A few very long rows among many short ones: the shapes where the split
+    path is faster, and where the cluster size floor (buffers at most 80 %
+    full at the gate's sampling floor) keeps the cluster path off its
+    overflow path."""
+    rng = np.random.default_rng(2200)
+    for lens, k in (([1 << 20] * 2 + [4096] * 62, 2048), ([1 << 22] + [16384] * 15, 2048),
+                    ([1 << 20] * 4 + [8192] * 124, 1024)):
+        S = max(lens)
+        scores = np.full((len(lens), S), np.inf, np.float32)
+        for b, L in enumerate(lens):
+            scores[b, :L] = workloads._round_bf16(rng.standard_normal(L).astype(np.float32))
+        table = workloads.permuted_table(rng, len(lens), workloads.pages_for(S, 64))
+        wl = workloads.Workload("skew", scores, np.asarray(lens, np.int32), table, 64, k, S, True)
+        with tuning(**({} if path == "auto" else split())):
+            out, raw, flags = run_gpu(wl)
+        compare(wl, out, raw)
+        assert flags == 0
