@@ -26,12 +26,16 @@
 // hand-out counter; every block resets its row's counters.
 //
 // Kernel 2 (persistent; a block claims segments from a global counter):
-//  1. Stream.  A block streams its segment with 16-byte loads; the segment
-//     it will take next is already being brought into L2 by a bulk prefetch.
-//     Keys above lo are appended to the row's candidate buffer as 64-bit
-//     composites (key << 32 | ~position), with one reservation per warp;
-//     keys equal to lo are only counted, per segment.  The block then fences
-//     its stores and counts the segment done for its row.
+//  1. Stream.  A block streams its segment with 16-byte loads, two steps in
+//     flight; the segment one round ahead (this one's index plus the grid
+//     size) is brought into L2 by a bulk prefetch.  A thread whose 16 values
+//     all lie below the gate float skips them after one compare; otherwise
+//     ties with lo are counted and keys above lo are staged, as 64-bit
+//     composites (key << 32 | ~position), in the warp's part of shared
+//     memory.  At the end of the segment each warp copies its staged
+//     composites to the row's candidate buffer with one reservation; the
+//     block fences its stores and counts the segment done for its row (the
+//     count's return is read one segment later).
 //  2. Resolve (the block whose segment completed the row):
 //     a. k <= n_gt <= capacity: the candidates are loaded into shared memory
 //        and the k largest composites found by 11-bit radix rounds over the
