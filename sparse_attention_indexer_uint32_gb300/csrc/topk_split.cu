@@ -34,8 +34,7 @@
 //     composites (key << 32 | ~position), in the warp's part of shared
 //     memory.  At the end of the segment each warp copies its staged
 //     composites to the row's candidate buffer with one reservation; the
-//     block fences its stores and counts the segment done for its row (the
-//     count's return is read one segment later).
+//     block fences its stores and counts the segment done for its row.
 //  2. Resolve (the block whose segment completed the row):
 //     a. k <= n_gt <= capacity: the candidates are loaded into shared memory
 //        and the k largest composites found by 11-bit radix rounds over the
@@ -594,8 +593,6 @@ __global__ void __launch_bounds__(kST, 2) split_select_kernel(const SplitParams 
     // in order, so the one a block will claim about one round from now is
     // near u + gridDim.x: that one is prefetched into L2 when segment u starts.
     uint32_t nxt = 0u;
-    int32_t pend_row = -1;  // thread 0: the row of the last segment counted, and its count's return
-    uint32_t pend_d = 0u;
     const uint32_t G = gridDim.x;
     if (tid == 0) {
         const uint32_t cur = atomicAdd(&p.ws.hdr->next_unit, 1u);
@@ -705,33 +702,16 @@ __global__ void __launch_bounds__(kST, 2) split_select_kernel(const SplitParams 
             s_eq = 0u;
             p.ws.unit_ties[cur] = e;
             if (e != 0u) atomicAdd(&p.ws.rows[row].n_eq, e);
-            // The previous segment's count (its atomic has returned by now)
-            // says whether that segment completed its row; this segment's
-            // count is issued now and read at the next boundary, so that no
-            // boundary waits for a round trip to L2.
-            s_res = -1;
-            if (pend_row >= 0 && pend_d + 1u == row_nunits[pend_row]) {
-                __threadfence();  // the other blocks' stores, before this block reads them
-                s_res = pend_row;
-            }
             __threadfence();
-            pend_d = atomicAdd(&p.ws.rows[row].done, 1u);
-            pend_row = row;
+            const uint32_t d = atomicAdd(&p.ws.rows[row].done, 1u);
+            const bool last = d + 1u == row_nunits[row];
+            if (last) __threadfence();  // the other blocks' stores, before this block reads them
+            s_res = last ? row : -1;
             s_cur = nxt;
         }
         __syncthreads();
         if (s_res >= 0) resolve(s_res);
     }
-    // The last segment's count.
-    if (tid == 0) {
-        s_res = -1;
-        if (pend_row >= 0 && pend_d + 1u == row_nunits[pend_row]) {
-            __threadfence();
-            s_res = pend_row;
-        }
-    }
-    __syncthreads();
-    if (s_res >= 0) resolve(s_res);
     if (tid == 0 && ctl.err != 0u) atomicOr(p.flags, ctl.err);
     // Dependents may start once every block has written its rows.
     __syncthreads();
