@@ -77,7 +77,9 @@ def test_tuning_roundtrip_and_validation(lib):
                            ("single_block_stages", 9), ("gate_refresh_tiles", -1), ("gate_refresh_tiles", 65),
                            ("warp_rows", 3), ("warp_rows", -1), ("long_threshold_large_batch", -1),
                            ("large_batch_min", -1), ("warp_batch_min", -1), ("stream_batch_min", -1), ("wait_limit_us", -1),
-                           ("wait_limit_us", 60000001), ("single_block_kernel", -1), ("single_block_kernel", 4)):
+                           ("wait_limit_us", 60000001), ("single_block_kernel", -1), ("single_block_kernel", 4),
+                           ("split_rows", 3), ("split_segment", 2048), ("split_segment", 12288),
+                           ("split_full_resolve", 2)):
             t2 = lib.topk_tuning_t(**old.as_dict())
             setattr(t2, field, bad)
             with pytest.raises(lib.TopkError) as e:
