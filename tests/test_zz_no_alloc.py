@@ -65,6 +65,22 @@ def test_no_alloc_matches_workspace_entry_point_on_two_calls():
         compare(wl, out, raw)  # and against the CPU oracle, row by row
 
 
+def test_no_alloc_on_the_segment_split_path():
+    """With the segment-split path asked for, the library's own array also
+    holds that path's row states and candidate buffers: a skewed batch and a
+    second, different one in a row, both against the oracle."""
+    from tests.parity_util import compare, tuning
+
+    cases = [
+        workloads.random_case(seed=73, batch=30, min_len=0, max_len=300000, k=1024, page_size=64, dist="bf16"),
+        workloads.random_case(seed=74, batch=128, min_len=1, max_len=20000, k=2048, page_size=16, dist="int"),
+    ]
+    with tuning(split_rows=1):
+        for wl in cases:
+            _, _, out, raw = _run_both(wl)
+            compare(wl, out, raw)
+
+
 def test_no_alloc_refuses_a_batch_above_its_limit():
     import torch
 
