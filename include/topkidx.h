@@ -287,14 +287,16 @@ typedef struct {
     int32_t split_rows;                 /* the segment-split path (the rows of the whole batch
                                            cut into segments that every SM streams; the block
                                            that finishes a row's last segment resolves it), for
-                                           batches of up to 128 rows: 1: always; 0 (automatic)
-                                           and 2: never.  On GB300 it is faster on batches that
-                                           mix a few very long rows with short ones (1 x 1M +
-                                           63 x 4K, k = 2048: 33 vs 39 us; 4 x 1M + 124 x 8K,
-                                           k = 1024: 34 vs 58 us) and slower on batches of
-                                           similar lengths (8 x 1M: 47 vs 33 us; 128 ragged rows
-                                           up to 256K: 63 vs 49 us); the host does not see the
-                                           lengths, so the caller chooses                        */
+                                           batches of up to 128 rows whose longest row keeps its
+                                           gated candidates within the path's per-row buffer
+                                           (about 2M tokens at k = 2048): 1: always; 0
+                                           (automatic) and 2: never.  On GB300 it is faster on
+                                           batches that mix a few very long rows with short ones
+                                           (1 x 1M + 63 x 4K, k = 2048: 33 vs 39 us; 4 x 1M +
+                                           124 x 8K, k = 1024: 34 vs 58 us) and slower on batches
+                                           of similar lengths (8 x 1M: 47 vs 33 us; 128 ragged
+                                           rows up to 256K: 63 vs 49 us); the host does not see
+                                           the lengths, so the caller chooses                    */
     int32_t split_segment;              /* 0: automatic; else a power of two, 4096..1048576:
                                            elements per segment of the split path (raised where
                                            the batch would need more than 16384 segments)        */

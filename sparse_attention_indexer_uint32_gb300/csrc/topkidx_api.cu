@@ -149,6 +149,33 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
     if (samples == 0 || samples > kMaxSamples) samples = kMaxSamples;
     c.samples = samples;
     c.smem = make_layout(cluster, c.tile, c.stages, c.cap, k).total;
+    if (cluster == 16 && t.candidate_capacity == 0) {
+        // The largest cluster on rows so long that the gate's sampling floor
+        // (about (E + 4 sqrt(E) + 4) L / M gated elements, E = M k / L) would
+        // fill a block's buffer past 80 %: a larger buffer, paid for with ring
+        // stages (1 x 16M, k = 2048: 57K gated, 3.6K per block).
+        const double L = static_cast<double>(max_seq_len);
+        const double M = static_cast<double>(samples);
+        const double E = M * static_cast<double>(k) / L;
+        const double per_block = (E + 4.0 * std::sqrt(E) + 4.0) * L / M / cluster;
+        if (per_block > 0.8 * c.cap) {
+            int dev = 0, optin = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            int want = static_cast<int>(std::ceil(per_block / 0.6 / 64.0)) * 64;
+            want = std::min(want, 16384);
+            int stages = c.stages;
+            while (stages > 2 && make_layout(cluster, c.tile, stages, want, k).total > static_cast<uint32_t>(optin))
+                --stages;
+            while (want > c.cap && make_layout(cluster, c.tile, stages, want, k).total > static_cast<uint32_t>(optin))
+                want -= 64;
+            if (want > c.cap) {
+                c.cap = want;
+                c.stages = stages;
+                c.smem = make_layout(cluster, c.tile, c.stages, c.cap, k).total;
+            }
+        }
+    }
     return c;
 }
 
@@ -221,6 +248,19 @@ int32_t split_segment(int32_t batch, int32_t max_seq_len, const topk_tuning_t& t
            seg <= (1 << 20))
         seg <<= 1;
     return seg <= (1 << 20) ? static_cast<int32_t>(seg) : 0;
+}
+
+// Whether a row of max_seq_len keeps the split path's per-row candidate
+// buffer (kSplitCap) at most 80 % full at its gate's sampling floor (about
+// (E + 4 sqrt(E) + 4) L / M gated elements, E = M k / L): rows up to about 2M
+// tokens at k = 2048.  Longer rows would overflow it into the one-block
+// full-row resolve (8 x 4M: 2.2 ms against 65 us on the cluster path).
+bool split_fits(int32_t max_seq_len, int32_t k, const topk_tuning_t& t) {
+    const double L = static_cast<double>(max_seq_len);
+    if (L <= 0.0) return true;
+    const double M = std::min(L, static_cast<double>(t.samples > 0 ? t.samples : kSplitMaxSamples));
+    const double E = M * static_cast<double>(k) / L;
+    return (E + 4.0 * std::sqrt(E) + 4.0) * L / M <= 0.8 * kSplitCap;
 }
 
 // Resident blocks of the warp-per-row kernel on the current device.
@@ -349,7 +389,7 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
     // k = 2048; 128 ragged rows up to 256K, k = 1024), because each segment
     // ends in a block barrier and a fenced count, and the gate is a kernel of
     // its own.
-    if (batch <= kSplitMaxRows && t.split_rows == 1) {
+    if (batch <= kSplitMaxRows && t.split_rows == 1 && split_fits(max_seq_len, k, t)) {
         const topk_status_t r = resident_split_units(&d->split_units);
         if (r != TOPK_OK) return r;
         d->split_seg = split_segment(batch, max_seq_len, t, d->split_units);

@@ -347,11 +347,13 @@ def test_mixed_batch_with_long_and_short_launches():
 def test_rows_far_past_one_million(path):
     """A 16M-token row, two rows of about 6M and a short one (k = 2048, a
     permuted table): the slice, tile and position arithmetic of the cluster
-    kernel (automatic: 16 blocks per row), of one block streaming a whole
-    64 MB row, and of the segment-split path, far past the workloads' 1M."""
+    kernel (automatic: 16 blocks per row, with the larger per-block buffer
+    such rows need) and of one block streaming a whole 64 MB row; for the
+    segment-split path, which takes rows of up to about 2M tokens at this k,
+    a 2M row, one of 1.5M and a short one."""
     rng = np.random.default_rng(2100)
-    S = 1 << 24
-    lens = [S, 6_000_001, 6_000_000 - 3, 777]
+    S = 1 << 24 if path != "split" else 1 << 21
+    lens = [S, 6_000_001, 6_000_000 - 3, 777] if path != "split" else [S, 1_500_001, 777]
     scores = np.full((len(lens), S), np.inf, np.float32)
     for b, L in enumerate(lens):
         scores[b, :L] = rng.standard_normal(L).astype(np.float32)

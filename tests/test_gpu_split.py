@@ -208,7 +208,7 @@ def test_skewed_batches(path):
     full at the gate's sampling floor) keeps the cluster path off its
     overflow path."""
     rng = np.random.default_rng(2200)
-    for lens, k in (([1 << 20] * 2 + [4096] * 62, 2048), ([1 << 22] + [16384] * 15, 2048),
+    for lens, k in (([1 << 20] * 2 + [4096] * 62, 2048), ([1 << 21] + [16384] * 15, 2048),
                     ([1 << 20] * 4 + [8192] * 124, 1024)):
         S = max(lens)
         scores = np.full((len(lens), S), np.inf, np.float32)
