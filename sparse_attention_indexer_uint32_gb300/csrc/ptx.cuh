@@ -204,6 +204,17 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for a barrier whose wait comes later than
+// its arrival (release on arrival, acquire on the wait).  Every thread of
+// every CTA in the cluster must execute both, in this order, before its next
+// cluster barrier.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_rank(uint32_t local_smem_addr, uint32_t rank) {
     uint32_t r;

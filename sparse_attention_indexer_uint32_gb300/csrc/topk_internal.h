@@ -156,6 +156,39 @@ struct SelectParams {
     uint64_t timeout_ns;
 };
 
+// What a select kernel reads of the plan before its first row: the header
+// check and the two work-list counts.  Every field is loaded before any is
+// tested, so the loads go out together (one trip to memory at the kernel's
+// start instead of two dependent ones).
+struct PlanView {
+    bool ok;          // the plan belongs to this batch (or there is none)
+    bool identity;    // item i is row i (the plan wrote no lists)
+    int32_t n_first;  // items taken from `items`
+    int32_t n_items;  // n_first + items taken from `items2`
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ PlanView read_plan(const SelectParams& p) {
+    uint32_t magic = kPlanMagic;
+    int32_t batch = p.batch, max_len = p.max_seq_len, identity = 0;
+    if (p.plan) {
+        magic = p.plan->magic;
+        batch = p.plan->batch;
+        max_len = p.plan->max_seq_len;
+        identity = p.plan->identity;
+    }
+    const int32_t a = p.n_items_dev ? *p.n_items_dev : p.n_items_host;
+    const int32_t b = p.items2 ? *p.n_items2_dev : 0;
+    PlanView v;
+    v.ok = magic == kPlanMagic && batch == p.batch && max_len == p.max_seq_len;
+    v.identity = p.plan != nullptr && identity != 0;
+    v.n_first = min(a, p.batch);
+    const int32_t n_second = p.items2 ? min(b, p.batch - v.n_first) : 0;
+    v.n_items = v.n_first + max(n_second, 0);
+    return v;
+}
+#endif
+
 // Parameters of the two kernels of the segment-split path.
 struct SplitParams {
     const float* scores;

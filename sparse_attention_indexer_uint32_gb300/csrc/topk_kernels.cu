@@ -126,22 +126,40 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
     clear_hist<NT>(s.hist_a, tid);
     clear_hist<NT>(s.hist_b, tid);
     __syncthreads();
-    if (C > 1) ptx::cluster_sync();  // every block of the cluster is running before any DSMEM access
+    // The cluster's start barrier is split: this block arrives now and waits
+    // just before its first access to another block's shared memory (the
+    // first histogram merge), so that the wait overlaps the prologue, the gate
+    // and pass 1.  Every block of the cluster is running before any DSMEM
+    // access.  (Block-uniform: every path to an exit goes through it.)
+    bool cl_arrived = false;
+    if (C > 1) {
+        ptx::cluster_arrive();
+        cl_arrived = true;
+    }
+    auto cluster_ready = [&]() {
+        if (C > 1 && cl_arrived) {
+            ptx::cluster_wait();
+            cl_arrived = false;
+        }
+    };
     // Every global access of this kernel comes after this point: the
     // preceding grid in the stream has completed and its writes are visible.
     ptx::grid_dependency_wait();
 
-    if (p.plan && (p.plan->magic != kPlanMagic || p.plan->batch != p.batch ||
-                   p.plan->max_seq_len != p.max_seq_len)) {
+    const PlanView pv = read_plan(p);
+    if (!pv.ok) {
         if (tid == 0 && rank == 0 && unit == 0) atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
+        cluster_ready();
         return;  // same for every block of a cluster
     }
-    const int32_t n_first = min(p.n_items_dev ? *p.n_items_dev : p.n_items_host, p.batch);
-    const bool identity = p.plan && p.plan->identity;  // the plan wrote no lists: item i is row i
-    const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
-    const int32_t n_items = n_first + max(n_second, 0);
+    const int32_t n_first = pv.n_first;
+    const bool identity = pv.identity;  // the plan wrote no lists: item i is row i
+    const int32_t n_items = pv.n_items;
     const int32_t my_items = snake_count(static_cast<int32_t>(unit), n_items, static_cast<int32_t>(nunits));
-    if (my_items <= 0) return;  // same for every block of a cluster
+    if (my_items <= 0) {
+        cluster_ready();
+        return;  // same for every block of a cluster
+    }
 
     const uint32_t K = static_cast<uint32_t>(p.k);
     const uint32_t cap = static_cast<uint32_t>(p.cap);
@@ -243,8 +261,12 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         // Initial fill: the stages are all free at a window boundary.  A block
         // whose wait gave up issues no more copies (a stage it gave up on may
         // still be receiving its copy).
-        if (tid == 0 && (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) == 0u) {
-            for (uint32_t t = win_base; t < win_end && t < win_base + stages; ++t) {
+        // Lane i of warp 0 issues the copy of stage i, so the first copies go
+        // out together.
+        if (warp == 0 && static_cast<uint32_t>(lane) < stages &&
+            (ptx::lds_u32(CTL(s, err)) & TOPK_FLAG_TIMEOUT) == 0u) {
+            const uint32_t t = win_base + static_cast<uint32_t>(lane);
+            if (t < win_end) {
                 ptx::sts_u32(s.claim + 4u * (t % stages), t / stages);
                 issue_tile(t, t % stages);
             }
@@ -588,6 +610,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
             uint32_t hm = s.hist_a;
             if (C > 1) {
                 if (tid == 0) ptx::sts_u32(s.hist_a + 4u * kSlotOverflow, local_ovf);
+                cluster_ready();
                 cluster_merge<NT, C>(s, s.hist_a, rank, tid);
                 hm = s.hist_m;
                 if (rank == 0 && tid == 0) {
@@ -1065,6 +1088,7 @@ __global__ void __launch_bounds__(NT, NT == 256 ? 3 : 2) select_kernel(const Sel
         }
     }
     if (C > 1) {
+        cluster_ready();
         ptx::cluster_sync();  // no block leaves while others may still address its shared memory
         // every rank is past its last output: rank 0 checks the last row's slot count
         if (rank == 0 && tid == 0 && erow > 0u &&

@@ -123,14 +123,14 @@ __global__ void __launch_bounds__(32 * (kStreamWarps + RW), RW == 4 ? 2 : 1) str
     // Every global access of this kernel comes after this point.
     ptx::grid_dependency_wait();
 
-    if (p.plan && (p.plan->magic != kPlanMagic || p.plan->batch != p.batch || p.plan->max_seq_len != p.max_seq_len)) {
+    const PlanView pv = read_plan(p);
+    if (!pv.ok) {
         if (tid == 0 && blockIdx.x == 0) atomicOr(p.flags, TOPK_FLAG_PLAN_MISMATCH);
         return;
     }
-    const int32_t n_first = min(p.n_items_dev ? *p.n_items_dev : p.n_items_host, p.batch);
-    const bool identity = p.plan && p.plan->identity;
-    const int32_t n_second = p.items2 ? min(*p.n_items2_dev, p.batch - n_first) : 0;
-    const int32_t n_items = n_first + max(n_second, 0);
+    const int32_t n_first = pv.n_first;
+    const bool identity = pv.identity;
+    const int32_t n_items = pv.n_items;
     const int32_t unit = static_cast<int32_t>(blockIdx.x), nunits = static_cast<int32_t>(gridDim.x);
     const int32_t my_items = snake_count(unit, n_items, nunits);
     if (my_items <= 0) return;
