@@ -377,6 +377,7 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                 // Key the buffered elements.  An element that passed the float
                 // compare but whose key is below the gate can only be a NaN; it
                 // gets key 0, which no later step selects.
+#pragma unroll 4
                 for (uint32_t i = lane; i < wcnt; i += 32u) {
                     const uint32_t key = score_key(__uint_as_float(ws.key[i]));
                     const uint32_t kept = key >= lo ? key : 0u;
@@ -403,12 +404,18 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
             for (int round = 0; round < 6; ++round) {
                 if (round > 0 && (r_lo == r_hi || cnt <= 32u)) break;
                 const int sh = wshift(r_hi - r_lo);
-                for (uint32_t i0 = 0; i0 < nbuf; i0 += 32u) {
-                    const uint32_t i = i0 + static_cast<uint32_t>(lane);
-                    if (i < nbuf) {
-                        const uint32_t key = ws.key[i];
-                        if (key >= r_lo && key <= r_hi && (key != 0u || !fillers))
-                            atomicAdd(&ws.hist[(key - r_lo) >> sh], 1u);
+                for (uint32_t i0 = 0; i0 < nbuf; i0 += 4u * 32u) {
+                    uint32_t kk[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                        kk[u] = i < nbuf ? ws.key[i] : 0u;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                        if (i < nbuf && kk[u] >= r_lo && kk[u] <= r_hi && (kk[u] != 0u || !fillers))
+                            atomicAdd(&ws.hist[(kk[u] - r_lo) >> sh], 1u);
                     }
                 }
                 __syncwarp();
@@ -498,11 +505,17 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
                 // Rounds over the buffer until one key or <= 32 entries.
                 for (int round = 0; round < 6 && r_lo != r_hi && cnt > 32u; ++round) {
                     const int sh = wshift(r_hi - r_lo);
-                    for (uint32_t i0 = 0; i0 < nbuf; i0 += 32u) {
-                        const uint32_t i = i0 + static_cast<uint32_t>(lane);
-                        if (i < nbuf) {
-                            const uint32_t key = ws.key[i];
-                            if (key >= r_lo && key <= r_hi) atomicAdd(&ws.hist[(key - r_lo) >> sh], 1u);
+                    for (uint32_t i0 = 0; i0 < nbuf; i0 += 4u * 32u) {
+                        uint32_t kk[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                            kk[u] = i < nbuf ? ws.key[i] : 0u;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                            if (i < nbuf && kk[u] >= r_lo && kk[u] <= r_hi) atomicAdd(&ws.hist[(kk[u] - r_lo) >> sh], 1u);
                         }
                     }
                     __syncwarp();
@@ -532,12 +545,21 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
             // copies, the smallest positions first (a position bitmap).
             const uint32_t T = r_lo;
             if (from_buffer) {
-                for (uint32_t i0 = 0; i0 < nbuf; i0 += 32u) {
-                    const uint32_t i = i0 + static_cast<uint32_t>(lane);
-                    const uint32_t key = i < nbuf ? ws.key[i] : 0u;
-                    const uint32_t pos = i < nbuf ? ws.pos[i] : 0u;
-                    emit(i < nbuf && key > T, pos);
-                    if (i < nbuf && key == T && (key != 0u || !fillers)) atomicOr(&ws.ties[pos >> 5], 1u << (pos & 31u));
+                for (uint32_t i0 = 0; i0 < nbuf; i0 += 4u * 32u) {
+                    uint32_t kk[4], pp[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                        kk[u] = i < nbuf ? ws.key[i] : 0u;
+                        pp[u] = i < nbuf ? ws.pos[i] : 0u;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                        emit(i < nbuf && kk[u] > T, pp[u]);
+                        if (i < nbuf && kk[u] == T && (kk[u] != 0u || !fillers))
+                            atomicOr(&ws.ties[pp[u] >> 5], 1u << (pp[u] & 31u));
+                    }
                 }
             } else {
                 for (uint32_t v0 = 0; v0 < nvec; v0 += 32u) {
@@ -592,24 +614,34 @@ __global__ void __launch_bounds__(kWarpThreads, 2) warp_select_kernel(const Sele
             // ---- at most 32 entries in [r_lo, r_hi] (from the buffer): above
             // the range is taken; the range's entries are ranked in the warp.
             uint32_t nf = 0;
-            for (uint32_t i0 = 0; i0 < nbuf; i0 += 32u) {
-                const uint32_t i = i0 + static_cast<uint32_t>(lane);
-                const uint32_t key = i < nbuf ? ws.key[i] : 0u;
-                const uint32_t pos = i < nbuf ? ws.pos[i] : 0u;
-                const bool live = i < nbuf && (key != 0u || !fillers);
-                emit(live && key > r_hi, pos);
-                const bool in = live && key >= r_lo && key <= r_hi;
-                const uint32_t m = __ballot_sync(kWFull, in);
-                if (in) {
-                    const uint32_t s = nf + static_cast<uint32_t>(__popc(m & lt));
-                    if (s < 32u) {
-                        ws.hist[s] = key;
-                        ws.hist[32u + s] = pos;
-                    } else {
-                        err |= TOPK_FLAG_INTERNAL;
-                    }
+            for (uint32_t i0 = 0; i0 < nbuf; i0 += 4u * 32u) {
+                // Four chunks' entries are loaded before any is used.
+                uint32_t kk[4], pp[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                    kk[u] = i < nbuf ? ws.key[i] : 0u;
+                    pp[u] = i < nbuf ? ws.pos[i] : 0u;
                 }
-                nf += static_cast<uint32_t>(__popc(m));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t i = i0 + 32u * u + static_cast<uint32_t>(lane);
+                    const uint32_t key = kk[u], pos = pp[u];
+                    const bool live = i < nbuf && (key != 0u || !fillers);
+                    emit(live && key > r_hi, pos);
+                    const bool in = live && key >= r_lo && key <= r_hi;
+                    const uint32_t m = __ballot_sync(kWFull, in);
+                    if (in) {
+                        const uint32_t s = nf + static_cast<uint32_t>(__popc(m & lt));
+                        if (s < 32u) {
+                            ws.hist[s] = key;
+                            ws.hist[32u + s] = pos;
+                        } else {
+                            err |= TOPK_FLAG_INTERNAL;
+                        }
+                    }
+                    nf += static_cast<uint32_t>(__popc(m));
+                }
             }
             __syncwarp();
             nf = min(nf, 32u);
