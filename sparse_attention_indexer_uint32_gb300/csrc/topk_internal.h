@@ -351,7 +351,9 @@ cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_o
 cudaError_t launch_page_transform(const int32_t* raw, int32_t batch, int32_t k, const int32_t* page_table,
                                   int64_t pt_stride, int32_t log2_page, int32_t* out, cudaStream_t stream);
 cudaError_t launch_key_map(const float* x, int64_t n, uint32_t* keys, cudaStream_t stream);
-cudaError_t launch_warp_select(const SelectParams& p, int grid, cudaStream_t stream);
+// programmatic: launched with programmatic stream serialization (its blocks
+// are placed while the plan finishes).
+cudaError_t launch_warp_select(const SelectParams& p, int grid, bool programmatic, cudaStream_t stream);
 // The warp-specialised single-block kernel (topk_stream.cu).
 // resolve_warps: 4 (two blocks per SM) or 8 (one block per SM).
 cudaError_t launch_stream_select(const SelectParams& p, int resolve_warps, int grid, size_t smem,

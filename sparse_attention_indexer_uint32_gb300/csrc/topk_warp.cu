@@ -705,7 +705,7 @@ cudaError_t warp_attributes(size_t smem) {
     return cudaSuccess;
 }
 
-cudaError_t launch_warp_select(const SelectParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_warp_select(const SelectParams& p, int grid, bool programmatic, cudaStream_t stream) {
     const size_t smem = warp_select_smem_bytes();
     const cudaError_t ea = warp_attributes(smem);
     if (ea != cudaSuccess) return ea;
@@ -716,7 +716,7 @@ cudaError_t launch_warp_select(const SelectParams& p, int grid, cudaStream_t str
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, warp_select_kernel, p);
