@@ -660,8 +660,11 @@ topk_status_t topk_transform(const float* scores, int64_t row_stride, const int3
         q.cap = sc.cap;
         q.samples = sc.samples;
         q.gate_fill = sc.gate_fill;
-        const int per_unit = (batch + stream_units - 1) / stream_units;
-        const int grid = (batch + per_unit - 1) / per_unit;
+        // Every resident block (not the fewest blocks with equal shares): the
+        // blocks that end up with one row fewer finish early and leave the
+        // others more of the memory bandwidth (384 x 32K: 27.4 vs 29.2 us;
+        // 1024 x 64K: 70.0 vs 72.9 us; 2048 x 64K unchanged).
+        const int grid = std::min(stream_units, batch);
         const cudaError_t e = launch_stream_select(q, sc.resolve_warps, grid, sc.smem, st);
         if (e != cudaSuccess) return cuda_fail(e, "stream select launch");
     } else if (!fold_short) {
