@@ -365,3 +365,24 @@ def test_rows_far_past_one_million(path):
         out, raw, flags = run_gpu(wl)
     compare(wl, out, raw)
     assert flags == 0
+
+
+def test_five_to_nine_very_long_rows():
+    """Five to nine rows of 512K tokens or more take 16-block clusters when
+    they fit the GPU at once (batch x 16 <= SMs), fewer-block ones past it;
+    the automatic dispatch on both sides of that bound, with ragged tails."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(2300)
+    for batch in (5, sms // 16, sms // 16 + 1):
+        S = 600_000
+        lens = [S - int(x) for x in rng.integers(0, 80_000, batch)]
+        scores = np.full((batch, S), np.inf, np.float32)
+        for b, L in enumerate(lens):
+            scores[b, :L] = workloads._round_bf16(rng.standard_normal(L).astype(np.float32))
+        table = workloads.permuted_table(rng, batch, workloads.pages_for(S, 64))
+        wl = workloads.Workload("few_long", scores, np.asarray(lens, np.int32), table, 64, 2048, S, True)
+        out, raw, flags = run_gpu(wl)
+        compare(wl, out, raw)
+        assert flags == 0
