@@ -401,8 +401,7 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
     if (!d->launch_long) return TOPK_OK;
     int cluster = t.cluster_size;
     if (cluster == 0) {
-        // 16 blocks per row for up to 4 rows (and up to 9 of 512K or more,
-        // below); then 4 for rows of at most 64K
+        // 16 blocks per row for up to 4 rows; then 4 for rows of at most 64K
         // (8 blocks would give each block 8K elements or fewer: 16 x 64K takes
         // 25.3 us with 8-block clusters and 21.5 us with 4-block ones, and 4 is
         // no slower at 4 or 8 rows); else 8 while every row gets a resident
@@ -412,10 +411,6 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
             cluster = 16;
         } else if (max_seq_len <= 65536) {
             cluster = 4;
-        } else if (max_seq_len >= 524288 && static_cast<int64_t>(batch) * 16 <= sm_count()) {
-            // Up to 9 rows of 512K or more: 16 blocks each (5 x 1M: 29.9 vs
-            // 32.9 us with 8 blocks; 6 x 1M: 30.0 vs 31.9; 8 x 1M: equal).
-            cluster = 16;
         } else {
             const PathConfig c8 = path_config(8, k, batch, max_seq_len, t);
             int u8 = 0;

@@ -367,10 +367,10 @@ def test_rows_far_past_one_million(path):
     assert flags == 0
 
 
-def test_five_to_nine_very_long_rows():
-    """Five to nine rows of 512K tokens or more take 16-block clusters when
-    they fit the GPU at once (batch x 16 <= SMs), fewer-block ones past it;
-    the automatic dispatch on both sides of that bound, with ragged tails."""
+def test_five_to_ten_very_long_rows():
+    """Five to ten rows of about 600K tokens through the automatic dispatch
+    (the cluster sizes it picks around one wave of 16-block clusters), with
+    ragged tails, bf16-rounded scores and a permuted table."""
     import torch
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
