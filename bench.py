@@ -405,9 +405,11 @@ def time_e2e(wl, steps: int, warmup: int, local: int, chunks: int = 4, copy_stre
     result device->host.  The batch is cut into `chunks` row ranges; each
     range's inputs go up on one of `copy_streams` copy streams, and its plan +
     transform + result copy run on the compute stream as soon as that range
-    has landed, so copies and selection overlap.  (On GB300 the host->device
-    copy runs near 200 GB/s whatever the number of copy streams, so the step
-    is copy-bound; 4 ranges on one copy stream measured best.)"""
+    has landed, so copies and selection overlap.  Consecutive steps overlap as
+    a serving loop's would: a range's next copy waits only until this step's
+    selection of that range is done with the device buffer.  (On GB300 the
+    host->device copy runs near 200 GB/s whatever the number of copy streams,
+    so the step is copy-bound; 4 ranges on one copy stream measured best.)"""
     import torch
 
     from sparse_attention_indexer_uint32_gb300 import _lib
@@ -428,13 +430,10 @@ def time_e2e(wl, steps: int, warmup: int, local: int, chunks: int = 4, copy_stre
     ws = [torch.zeros(_lib.topk_plan_workspace_bytes(b - a), dtype=torch.uint8, device=dev) for a, b in ranges]
     landed = [torch.cuda.Event() for _ in ranges]
     freed = [torch.cuda.Event() for _ in ranges]
-    start = torch.cuda.Event()
 
     def step():
-        start.record(comp)
         for i, (a, b) in enumerate(ranges):
             cs = cstreams[i % len(cstreams)]
-            cs.wait_event(start)
             cs.wait_event(freed[i])  # the previous step's selection of this range is done with its inputs
             with torch.cuda.stream(cs):
                 d_scores[a:b].copy_(h_scores[a:b], non_blocking=True)
@@ -456,6 +455,8 @@ def time_e2e(wl, steps: int, warmup: int, local: int, chunks: int = 4, copy_stre
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
+    for cs in cstreams:  # no copy of the timed steps starts before e0
+        cs.wait_event(e0)
     for _ in range(steps):
         step()
     e1.record(comp)  # the compute stream waited for every range's copy
