@@ -1439,6 +1439,7 @@ cudaError_t launch_select(const SelectParams& p, int cluster, int threads, int g
     switch (cluster) {
         case 1: return launch_select_c<1>(p, threads, grid_units, smem, stream);
         case 2: return launch_select_c<2>(p, threads, grid_units, smem, stream);
+        case 3: return launch_select_c<3>(p, threads, grid_units, smem, stream);
         case 4: return launch_select_c<4>(p, threads, grid_units, smem, stream);
         case 8: return launch_select_c<8>(p, threads, grid_units, smem, stream);
         case 16: return launch_select_c<16>(p, threads, grid_units, smem, stream);
@@ -1450,6 +1451,7 @@ cudaError_t select_occupancy(int cluster, int threads, size_t smem, int* units_o
     switch (cluster) {
         case 1: return occupancy_c<1>(threads, smem, units_out);
         case 2: return occupancy_c<2>(threads, smem, units_out);
+        case 3: return occupancy_c<3>(threads, smem, units_out);
         case 4: return occupancy_c<4>(threads, smem, units_out);
         case 8: return occupancy_c<8>(threads, smem, units_out);
         case 16: return occupancy_c<16>(threads, smem, units_out);

@@ -71,7 +71,7 @@ def test_tuning_roundtrip_and_validation(lib):
         t.wait_limit_us = 1
         lib.topk_set_tuning(t)
         assert lib.topk_get_tuning().wait_limit_us == 1
-        for field, bad in (("cluster_size", 3), ("candidate_capacity", 100), ("samples", 33),
+        for field, bad in (("cluster_size", 5), ("candidate_capacity", 100), ("samples", 33),
                            ("long_threshold", -1), ("gate_fill_percent", 101), ("gate_fill_percent", -1),
                            ("single_block_threads", 128), ("single_block_copy_bytes", 4096), ("single_block_stages", 1),
                            ("single_block_stages", 9), ("gate_refresh_tiles", -1), ("gate_refresh_tiles", 65),

@@ -95,7 +95,7 @@ def test_random_ragged_single_block(dist, k):
 
 
 @pytest.mark.parametrize("batch", [3, 40])  # few rows: 512-thread blocks, 32 KB copies; many: 256, 16 KB
-@pytest.mark.parametrize("cluster", [2, 4, 8, 16])
+@pytest.mark.parametrize("cluster", [2, 3, 4, 8, 16])
 @pytest.mark.parametrize("dist", ["normal", "bf16", "flat", "neginf"])
 def test_cluster_path_forced(cluster, dist, batch):
     wl = workloads.random_case(seed=100 + cluster + batch, batch=batch, min_len=1, max_len=70001, k=700,
@@ -383,6 +383,20 @@ def test_five_to_ten_very_long_rows():
             scores[b, :L] = workloads._round_bf16(rng.standard_normal(L).astype(np.float32))
         table = workloads.permuted_table(rng, batch, workloads.pages_for(S, 64))
         wl = workloads.Workload("few_long", scores, np.asarray(lens, np.int32), table, 64, 2048, S, True)
+        out, raw, flags = run_gpu(wl)
+        compare(wl, out, raw)
+        assert flags == 0
+
+
+def test_three_block_clusters_on_long_mixes():
+    """Batches of long rows that 4-block clusters would double up on take
+    3-block clusters (the slice arithmetic of a cluster size that does not
+    divide the row in powers of two), through the automatic dispatch: a
+    ragged mix, and uniform long rows with k = 2048 near the buffer floor."""
+    rng = np.random.default_rng(2400)
+    for batch, lo, hi, k, dist in ((100, 1024, 262144, 1024, "normal"), (160, 70001, 300001, 2048, "bf16")):
+        wl = workloads.random_case(seed=int(rng.integers(1 << 30)), batch=batch, min_len=lo, max_len=hi, k=k,
+                                   page_size=64, dist=dist)
         out, raw, flags = run_gpu(wl)
         compare(wl, out, raw)
         assert flags == 0
