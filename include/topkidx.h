@@ -233,11 +233,8 @@ typedef struct {
     int32_t small_batch_max;            /* (16)                                                  */
     int32_t cluster_size;               /* blocks per long row: 2, 3, 4, 8 or 16; 0: automatic
                                            (16 for up to 4 rows; else 4 for rows of at most 64K;
-                                           else 8 while every row gets a resident 8-block cluster;
-                                           else 3 when 4-block clusters would take two rows on
-                                           some cluster and the batch is at most two waves of
-                                           3-block ones, else 4; then raised (3 to 4, then
-                                           doubled) while a row of max_seq_len would
+                                           else 8 while every row gets a resident 8-block cluster,
+                                           else 4; then doubled while a row of max_seq_len would
                                            fill a block's candidate buffer past 80 % at the
                                            gate's sampling floor)                                */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every

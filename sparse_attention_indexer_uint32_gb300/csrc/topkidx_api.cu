@@ -416,22 +416,7 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
             int u8 = 0;
             const topk_status_t r = resident_units(8, c8.threads, c8.smem, &u8);
             if (r != TOPK_OK) return r;
-            if (batch <= u8) {
-                cluster = 8;
-            } else {
-                // 3 blocks per row where 4-block clusters would give some
-                // cluster two rows and 3-block ones fewer do (up to two waves
-                // of them): the ragged mix of 128 rows up to 256K takes 45.2
-                // vs 48.3 us, 100 rows of U[1K, 256K] 36.0 vs 40.1; 128 rows
-                // of U[128K, 256K] 57.4 vs 56.4, 200 of U[70K, 300K] equal.
-                const PathConfig c4 = path_config(4, k, batch, max_seq_len, t);
-                const PathConfig c3 = path_config(3, k, batch, max_seq_len, t);
-                int u4 = 0, u3 = 0;
-                topk_status_t r2 = resident_units(4, c4.threads, c4.smem, &u4);
-                if (r2 == TOPK_OK) r2 = resident_units(3, c3.threads, c3.smem, &u3);
-                if (r2 != TOPK_OK) return r2;
-                cluster = (batch > u4 && batch <= 2 * u3) ? 3 : 4;
-            }
+            cluster = batch <= u8 ? 8 : 4;
         }
     }
     if (t.cluster_size == 0) {
@@ -448,7 +433,7 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
         const double E = M * static_cast<double>(k) / L;
         const double gated = (E + 4.0 * std::sqrt(E) + 4.0) * L / M;
         const double cap = static_cast<double>(path_config(cluster, k, batch, max_seq_len, t).cap);
-        while (cluster < 16 && gated / cluster > 0.8 * cap) cluster = cluster == 3 ? 4 : 2 * cluster;
+        while (cluster < 16 && gated / cluster > 0.8 * cap) cluster *= 2;
     }
     d->cl = path_config(cluster, k, batch, max_seq_len, t);
     const topk_status_t r = resident_units(d->cl.cluster, d->cl.threads, d->cl.smem, &d->cl_units);

@@ -389,14 +389,14 @@ def test_five_to_ten_very_long_rows():
 
 
 def test_three_block_clusters_on_long_mixes():
-    """Batches of long rows that 4-block clusters would double up on take
-    3-block clusters (the slice arithmetic of a cluster size that does not
-    divide the row in powers of two), through the automatic dispatch: a
-    ragged mix, and uniform long rows with k = 2048 near the buffer floor."""
+    """3-block clusters (asked for: a cluster size that does not split rows in
+    powers of two) on batches of long rows that give clusters two rows: a
+    ragged mix, and rows of 70K-300K with k = 2048 near the buffer floor."""
     rng = np.random.default_rng(2400)
     for batch, lo, hi, k, dist in ((100, 1024, 262144, 1024, "normal"), (160, 70001, 300001, 2048, "bf16")):
         wl = workloads.random_case(seed=int(rng.integers(1 << 30)), batch=batch, min_len=lo, max_len=hi, k=k,
                                    page_size=64, dist=dist)
-        out, raw, flags = run_gpu(wl)
+        with tuning(cluster_size=3):
+            out, raw, flags = run_gpu(wl)
         compare(wl, out, raw)
         assert flags == 0
