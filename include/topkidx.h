@@ -233,15 +233,21 @@ typedef struct {
     int32_t small_batch_max;            /* (16)                                                  */
     int32_t cluster_size;               /* blocks per long row: 2, 3, 4, 8 or 16; 0: automatic
                                            (16 for up to 4 rows; else 4 for rows of at most 64K;
-                                           else 8 while every row gets a resident 8-block cluster,
-                                           else 4; then doubled while a row of max_seq_len would
-                                           fill a block's candidate buffer past 80 % at the
-                                           gate's sampling floor)                                */
+                                           else 8 while every row gets a resident 8-block cluster;
+                                           else 3 when 4-block clusters would take two rows on
+                                           some cluster, the batch is at most two waves of
+                                           3-block ones and a 3-block buffer holds the gate's
+                                           sampling floor at 40 %; else 4; then raised (3 to 4,
+                                           then doubled) while a row of max_seq_len would fill a
+                                           buffer of max(k, 2048) past 80 % at that floor)       */
     int32_t force_two_pass;             /* 1: no candidate buffering in the first pass, so every
                                            row takes the two-pass streaming path                  */
     int32_t disable_gate;               /* 1: the first pass counts every element (no sample gate) */
-    int32_t candidate_capacity;         /* 0: automatic; else candidates per block, 2048..16384,
-                                           a multiple of 64                                      */
+    int32_t candidate_capacity;         /* 0: automatic (single blocks 4k, at least 2048, 3072
+                                           on rows over 16K; clusters max(k, 2048), grown toward
+                                           2.5 times the gate's sampling floor per block where the
+                                           shared memory at the same blocks per SM allows); else
+                                           candidates per block, 2048..16384, a multiple of 64    */
     int32_t samples;                    /* 0: automatic; else at most this many gate samples per
                                            row, 32..2048, a multiple of 32                       */
     int32_t gate_fill_percent;          /* 0: automatic; else 1..100: the gate is loosened until it

@@ -98,7 +98,22 @@ int sm_count() {
 // shared memory that keeps two or three blocks per SM.  Single blocks: a
 // candidate buffer of 4k entries (>= 2048; >= 3072 for rows over 16K).
 // Clusters: a k-entry buffer (>= 2048).
-PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_len, const topk_tuning_t& t) {
+topk_status_t resident_units(int cluster, int threads, size_t smem, int* units);
+
+// Gated elements per block of a C-block cluster at the gate's sampling floor:
+// r = E + 4 sqrt(E) + 4 of M samples (E = M k / L) stands for r L / M
+// elements of a row of L.
+double floor_per_block(int cluster, int32_t k, int32_t max_seq_len, int samples) {
+    const double L = static_cast<double>(max_seq_len);
+    const double M = std::min(static_cast<double>(samples), L);
+    const double E = M * static_cast<double>(std::min(k, max_seq_len)) / L;
+    return (E + 4.0 * std::sqrt(E) + 4.0) * L / M / cluster;
+}
+
+// grow_buffer = false: the cluster buffer before it is sized to the gate's
+// sampling floor (the dispatch's cluster-size floor reasons on that one).
+PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_len, const topk_tuning_t& t,
+                       bool grow_buffer = true) {
     PathConfig c;
     c.cluster = cluster;
     const bool few_rows = cluster > 1 && static_cast<int64_t>(batch) * cluster * 2 <= sm_count();
@@ -149,15 +164,44 @@ PathConfig path_config(int cluster, int32_t k, int32_t batch, int32_t max_seq_le
     if (samples == 0 || samples > kMaxSamples) samples = kMaxSamples;
     c.samples = samples;
     c.smem = make_layout(cluster, c.tile, c.stages, c.cap, k).total;
+    if (cluster > 1 && t.candidate_capacity == 0 && grow_buffer) {
+        // The gate's count spreads with its sampled rank r (about 1/sqrt(r)
+        // of the count, the same way in every block of the row), and a block
+        // whose buffer overflows sends its cluster's row through re-reads of
+        // the slices, tens of microseconds.  Where the sampling floor alone
+        // fills a block's buffer past 40 %, the buffer grows toward that
+        // share, within the shared memory left at the same blocks per SM
+        // (3-block clusters on 256K rows at k = 1024 gate about 1024
+        // elements per block: with 2048 entries one row in a few hundred
+        // overflowed, and a batch of 190 such rows took 126 us instead of 65).
+        const double per_block = floor_per_block(cluster, k, max_seq_len, samples);
+        if (per_block > 0.4 * c.cap) {
+            int dev = 0, optin = 0, per_sm = 0, reserved = 0, base = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+            const int blocks = std::max(1, per_sm / (static_cast<int>(c.smem) + reserved));
+            const int budget = std::min(optin, per_sm / blocks - reserved);
+            int want = std::min(16384, static_cast<int>(std::ceil(per_block / 0.4 / 64.0)) * 64);
+            while (want > c.cap && make_layout(cluster, c.tile, c.stages, want, k).total > static_cast<uint32_t>(budget))
+                want -= 64;
+            if (want > c.cap && resident_units(cluster, c.threads, c.smem, &base) == TOPK_OK) {
+                const size_t grown = make_layout(cluster, c.tile, c.stages, want, k).total;
+                int units = 0;
+                if (resident_units(cluster, c.threads, grown, &units) == TOPK_OK && units >= base) {
+                    c.cap = want;
+                    c.smem = grown;
+                }
+            }
+        }
+    }
     if (cluster == 16 && t.candidate_capacity == 0) {
         // The largest cluster on rows so long that the gate's sampling floor
-        // (about (E + 4 sqrt(E) + 4) L / M gated elements, E = M k / L) would
-        // fill a block's buffer past 80 %: a larger buffer, paid for with ring
-        // stages (1 x 16M, k = 2048: 57K gated, 3.6K per block).
-        const double L = static_cast<double>(max_seq_len);
-        const double M = static_cast<double>(samples);
-        const double E = M * static_cast<double>(k) / L;
-        const double per_block = (E + 4.0 * std::sqrt(E) + 4.0) * L / M / cluster;
+        // would fill a block's buffer past 80 % even so: a larger buffer,
+        // paid for with ring stages (1 x 16M, k = 2048: 57K gated, 3.6K per
+        // block).
+        const double per_block = floor_per_block(cluster, k, max_seq_len, samples);
         if (per_block > 0.8 * c.cap) {
             int dev = 0, optin = 0;
             cudaGetDevice(&dev);
@@ -365,8 +409,8 @@ topk_status_t resident_stream_units(int resolve_warps, size_t smem, int* units) 
 // The kernels one topk_transform call launches.  Long rows go to the cluster
 // kernel.  Blocks per row (cluster_size 0): 16 while the rows take at most
 // one SM per block that way, 8 while every row gets a resident cluster at
-// once, else 4 (or 8 again when the sampled gate's floor would crowd a
-// 4-block cluster's candidate buffers).  When the whole batch fits in two
+// once, else 3 or 4 (raised when the sampled gate's floor would crowd the
+// clusters' candidate buffers).  When the whole batch fits in two
 // waves of those clusters, the short rows are handed to the
 // cluster kernel as well (after the long ones), so that no second launch runs
 // after it.
@@ -416,7 +460,26 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
             int u8 = 0;
             const topk_status_t r = resident_units(8, c8.threads, c8.smem, &u8);
             if (r != TOPK_OK) return r;
-            cluster = batch <= u8 ? 8 : 4;
+            if (batch <= u8) {
+                cluster = 8;
+            } else {
+                // 3 blocks per row where 4-block clusters would give some
+                // cluster two rows and 3-block ones fewer do (up to two waves
+                // of them): the ragged mix of 128 rows up to 256K took 46.2
+                // vs 48.2 us, 150 bf16 rows of U[1K, 256K] 52.3 vs 85.1, 190
+                // rows of 256K 64.6 vs 83.0; rows of one length that fill
+                // one wave of 4-block clusters and a part of the next lose
+                // (128 x 256K: 60.5 vs 54.4).  Only where a 3-block buffer
+                // holds the gate's sampling floor at 40 %.
+                const PathConfig c4 = path_config(4, k, batch, max_seq_len, t);
+                const PathConfig c3 = path_config(3, k, batch, max_seq_len, t);
+                int u4 = 0, u3 = 0;
+                topk_status_t r2 = resident_units(4, c4.threads, c4.smem, &u4);
+                if (r2 == TOPK_OK) r2 = resident_units(3, c3.threads, c3.smem, &u3);
+                if (r2 != TOPK_OK) return r2;
+                const bool fits = floor_per_block(3, k, max_seq_len, c3.samples) <= 0.4 * c3.cap;
+                cluster = (fits && batch > u4 && batch <= 2 * u3) ? 3 : 4;
+            }
         }
     }
     if (t.cluster_size == 0) {
@@ -432,8 +495,8 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
         const double M = static_cast<double>(t.samples > 0 && t.samples < kMaxSamples ? t.samples : kMaxSamples);
         const double E = M * static_cast<double>(k) / L;
         const double gated = (E + 4.0 * std::sqrt(E) + 4.0) * L / M;
-        const double cap = static_cast<double>(path_config(cluster, k, batch, max_seq_len, t).cap);
-        while (cluster < 16 && gated / cluster > 0.8 * cap) cluster *= 2;
+        const double cap = static_cast<double>(path_config(cluster, k, batch, max_seq_len, t, false).cap);
+        while (cluster < 16 && gated / cluster > 0.8 * cap) cluster = cluster == 3 ? 4 : 2 * cluster;
     }
     d->cl = path_config(cluster, k, batch, max_seq_len, t);
     const topk_status_t r = resident_units(d->cl.cluster, d->cl.threads, d->cl.smem, &d->cl_units);
