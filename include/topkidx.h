@@ -235,7 +235,7 @@ typedef struct {
                                            (16 for up to 4 rows; else 4 for rows of at most 64K;
                                            else 8 while every row gets a resident 8-block cluster;
                                            else 3 when 4-block clusters would take two rows on
-                                           some cluster, the batch is at most two waves of
+                                           some cluster, the batch is at most four waves of
                                            3-block ones and a 3-block buffer holds the gate's
                                            sampling floor at 40 %; else 4; then raised (3 to 4,
                                            then doubled) while a row of max_seq_len would fill a

@@ -411,9 +411,9 @@ topk_status_t resident_stream_units(int resolve_warps, size_t smem, int* units) 
 // one SM per block that way, 8 while every row gets a resident cluster at
 // once, else 3 or 4 (raised when the sampled gate's floor would crowd the
 // clusters' candidate buffers).  When the whole batch fits in two
-// waves of those clusters, the short rows are handed to the
-// cluster kernel as well (after the long ones), so that no second launch runs
-// after it.
+// waves of those clusters (four of automatic 3-block ones), the short rows
+// are handed to the cluster kernel as well (after the long ones), so that no
+// second launch runs after it.
 struct Dispatch {
     bool launch_long = false;
     bool fold_short = false;
@@ -464,13 +464,14 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
                 cluster = 8;
             } else {
                 // 3 blocks per row where 4-block clusters would give some
-                // cluster two rows and 3-block ones fewer do (up to two waves
-                // of them): the ragged mix of 128 rows up to 256K took 46.2
-                // vs 48.2 us, 150 bf16 rows of U[1K, 256K] 52.3 vs 85.1, 190
-                // rows of 256K 64.6 vs 83.0; rows of one length that fill
-                // one wave of 4-block clusters and a part of the next lose
-                // (128 x 256K: 60.5 vs 54.4).  Only where a 3-block buffer
-                // holds the gate's sampling floor at 40 %.
+                // cluster two rows, up to four waves of 3-block clusters in
+                // one launch: the ragged mix of 128 rows up to 256K took
+                // 46.2 vs 48.2 us, 150 bf16 rows of U[1K, 256K] 52.3 vs 85.1,
+                // 300 of them 79.0 vs 94.4, 256 rows of 256K 90.2 vs 101.5;
+                // rows of one length that fill one wave of 4-block clusters
+                // and a part of the next lose (128 x 256K: 60.5 vs 54.4).
+                // Only where a 3-block buffer holds the gate's sampling floor
+                // at 40 %.
                 const PathConfig c4 = path_config(4, k, batch, max_seq_len, t);
                 const PathConfig c3 = path_config(3, k, batch, max_seq_len, t);
                 int u4 = 0, u3 = 0;
@@ -478,7 +479,7 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
                 if (r2 == TOPK_OK) r2 = resident_units(3, c3.threads, c3.smem, &u3);
                 if (r2 != TOPK_OK) return r2;
                 const bool fits = floor_per_block(3, k, max_seq_len, c3.samples) <= 0.4 * c3.cap;
-                cluster = (fits && batch > u4 && batch <= 2 * u3) ? 3 : 4;
+                cluster = (fits && batch > u4 && batch <= 4 * u3) ? 3 : 4;
             }
         }
     }
@@ -501,7 +502,11 @@ topk_status_t decide_dispatch(int32_t batch, int32_t max_seq_len, int32_t k, con
     d->cl = path_config(cluster, k, batch, max_seq_len, t);
     const topk_status_t r = resident_units(d->cl.cluster, d->cl.threads, d->cl.smem, &d->cl_units);
     if (r != TOPK_OK) return r;
-    d->fold_short = static_cast<int64_t>(batch) <= 2 * static_cast<int64_t>(d->cl_units);
+    // Short rows join the cluster launch while the batch is at most two waves
+    // of clusters (four of the automatic 3-block ones): one launch instead of
+    // a second one after it.
+    d->fold_short = static_cast<int64_t>(batch) <= (d->cl.cluster == 3 && t.cluster_size == 0 ? 4 : 2) *
+                                                       static_cast<int64_t>(d->cl_units);
     return TOPK_OK;
 }
 

@@ -391,12 +391,13 @@ def test_five_to_ten_very_long_rows():
 def test_three_block_clusters_on_long_mixes():
     """3-block clusters (a cluster size that does not split rows in powers of
     two) on batches of long rows that give 4-block clusters two rows, through
-    the automatic dispatch (which takes them for the ragged mix at k = 1024)
-    and asked for (rows of 70K-300K with k = 2048, where the automatic
-    dispatch keeps 4 blocks: a 3-block buffer would not hold the gate's floor
-    at 40 %)."""
+    the automatic dispatch (which takes them for a ragged mix at k = 1024,
+    and for 260 mixed rows at k = 512: three waves in one launch) and asked
+    for (rows of 70K-300K with k = 2048, where the automatic dispatch keeps
+    4 blocks: a 3-block buffer would not hold the gate's floor at 40 %)."""
     rng = np.random.default_rng(2400)
-    for batch, lo, hi, k, dist in ((100, 1024, 262144, 1024, "normal"), (160, 70001, 300001, 2048, "bf16")):
+    for batch, lo, hi, k, dist in ((100, 1024, 262144, 1024, "normal"), (160, 70001, 300001, 2048, "bf16"),
+                                   (260, 1024, 262144, 512, "bf16")):
         wl = workloads.random_case(seed=int(rng.integers(1 << 30)), batch=batch, min_len=lo, max_len=hi, k=k,
                                    page_size=64, dist=dist)
         out, raw, flags = run_gpu(wl)
